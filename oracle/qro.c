@@ -1,0 +1,408 @@
+/*
+ * qro.c -- CPU oracle for the quick-allreduce codec and emulated allreduce.
+ *
+ * TEST INFRASTRUCTURE ONLY (see qro.h).  Plain loops, one block at a time,
+ * every floating-point step an explicit IEEE binary32 operation.  Build with
+ * contraction off (-ffp-contract=off) and without fast-math, so that no
+ * a*b+c is fused and no operation is reordered: the result of each line below
+ * is the rounded result the comment names.
+ *
+ * Notation: "+", "-", "*", "/" on float below are IEEE binary32 operations in
+ * round-to-nearest-even.  h(v) = binary32 -> fp16, round-half-to-even,
+ * saturating to +-65504.  d(v) = binary32 -> output dtype (fp16 or bf16),
+ * round-half-to-even, IEEE overflow to infinity.
+ */
+#include "qro.h"
+
+#include <math.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Binary floating-point formats, written from their definitions:            */
+/* value = (-1)^s * 2^(e - bias) * (1 + m / 2^(p-1)) for 0 < e,               */
+/* value = (-1)^s * 2^(emin) * (m / 2^(p-1)) for e == 0 (subnormal),          */
+/* with p significand bits (implicit bit included).                          */
+/*   fp16  (IEEE binary16): p = 11, bias 15, emin -14, max 65504, e=31 inf    */
+/*   bf16  (bfloat16):      p = 8,  bias 127, emin -126, e=255 inf            */
+/*   e4m3fn (OCP FP8):      p = 4,  bias 7, emin -6, max 448, no infinity,    */
+/*                          e=15,m=7 is NaN                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Round a finite non-negative value to the nearest multiple of the format's
+ * quantum at its binade, ties to the even multiple.  The quantum is
+ * 2^(max(E, emin) - (p - 1)) with E = floor(log2 v).  Exact in double for any
+ * binary32 input. */
+static double round_to_format(double v, int p, int emin) {
+  if (v == 0.0) return 0.0;
+  int E;
+  (void)frexp(v, &E); /* v = f * 2^E with f in [0.5, 1) */
+  E -= 1;             /* now 2^E <= v < 2^(E+1) */
+  if (E < emin) E = emin;
+  int qexp = E - (p - 1);
+  double scaled = ldexp(v, -qexp); /* exact: a power-of-two scaling */
+  double k = floor(scaled);
+  double frac = scaled - k; /* exact */
+  if (frac > 0.5 || (frac == 0.5 && fmod(k, 2.0) != 0.0)) k += 1.0;
+  return ldexp(k, qexp);
+}
+
+/* Bit pattern (without sign) of a non-negative value already representable in
+ * the format. */
+static unsigned encode_fields(double a, int p, int emin, int bias) {
+  if (a == 0.0) return 0u;
+  int E;
+  (void)frexp(a, &E);
+  E -= 1;
+  if (E < emin) { /* subnormal: exponent field 0 */
+    double m = ldexp(a, -(emin - (p - 1)));
+    return (unsigned)m;
+  }
+  double m = ldexp(a, -(E - (p - 1))) - ldexp(1.0, p - 1);
+  return ((unsigned)(E + bias) << (p - 1)) | (unsigned)m;
+}
+
+static double decode_fields(unsigned e, unsigned m, int p, int emin, int bias) {
+  if (e == 0) return ldexp((double)m, emin - (p - 1));
+  return ldexp((double)((1u << (p - 1)) + m), (int)e - bias - (p - 1));
+}
+
+float qro_f16_to_f32(uint16_t h) {
+  unsigned s = h >> 15, e = (h >> 10) & 0x1Fu, m = h & 0x3FFu;
+  double v;
+  if (e == 31) v = m ? NAN : INFINITY;
+  else v = decode_fields(e, m, 11, -14, 15);
+  return (float)(s ? -v : v);
+}
+
+static uint16_t f32_to_f16_impl(float v, int saturate) {
+  unsigned sign = signbit(v) ? 0x8000u : 0u;
+  if (isnan(v)) return (uint16_t)(sign | 0x7E00u);
+  double a = fabs((double)v);
+  double r = isinf(v) ? INFINITY : round_to_format(a, 11, -14);
+  if (r > 65504.0) {
+    if (saturate) return (uint16_t)(sign | 0x7BFFu); /* 65504 */
+    return (uint16_t)(sign | 0x7C00u);                /* infinity */
+  }
+  return (uint16_t)(sign | encode_fields(r, 11, -14, 15));
+}
+
+uint16_t qro_f32_to_f16(float v) { return f32_to_f16_impl(v, 0); }
+uint16_t qro_f32_to_f16_satfinite(float v) { return f32_to_f16_impl(v, 1); }
+
+float qro_bf16_to_f32(uint16_t h) {
+  unsigned s = h >> 15, e = (h >> 7) & 0xFFu, m = h & 0x7Fu;
+  double v;
+  if (e == 255) v = m ? NAN : INFINITY;
+  else v = decode_fields(e, m, 8, -126, 127);
+  return (float)(s ? -v : v);
+}
+
+uint16_t qro_f32_to_bf16(float v) {
+  unsigned sign = signbit(v) ? 0x8000u : 0u;
+  if (isnan(v)) return (uint16_t)(sign | 0x7FC0u);
+  double a = fabs((double)v);
+  double r = isinf(v) ? INFINITY : round_to_format(a, 8, -126);
+  double bf16_max = ldexp(255.0, 127 - 7); /* (2 - 2^-7) * 2^127 */
+  if (r > bf16_max) return (uint16_t)(sign | 0x7F80u);
+  return (uint16_t)(sign | encode_fields(r, 8, -126, 127));
+}
+
+float qro_e4m3_to_f32(uint8_t c) {
+  unsigned s = c >> 7, e = (c >> 3) & 0xFu, m = c & 0x7u;
+  double v;
+  if (e == 15 && m == 7) v = NAN;
+  else v = decode_fields(e, m, 4, -6, 7);
+  return (float)(s ? -v : v);
+}
+
+uint8_t qro_f32_to_e4m3_satfinite(float v) {
+  unsigned sign = signbit(v) ? 0x80u : 0u;
+  if (isnan(v)) return (uint8_t)(sign | 0x7Fu);
+  double a = fabs((double)v);
+  double r = isinf(v) ? INFINITY : round_to_format(a, 4, -6);
+  if (r > 448.0) r = 448.0;
+  return (uint8_t)(sign | encode_fields(r, 4, -6, 7));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Formats.  Per 32-element block: b-bit codes (b = 8, 6 or 4), an fp16 scale */
+/* and, for the asymmetric formats, an fp16 zero-point.                      */
+/* ------------------------------------------------------------------------ */
+
+static int code_bits(int fmt) {
+  switch (fmt) {
+    case QRO_Q8: case QRO_FP8: case QRO_Q8A: return 8;
+    case QRO_Q6: return 6;
+    case QRO_Q4: case QRO_Q4A: return 4;
+    default: return 0;
+  }
+}
+static int is_asym(int fmt) { return fmt == QRO_Q8A || fmt == QRO_Q4A; }
+static int is_quantized(int fmt) { return code_bits(fmt) != 0; }
+/* Symmetric integer formats use codes -Qmax..Qmax with Qmax = 2^(b-1) - 1. */
+static int sym_qmax(int fmt) { return (1 << (code_bits(fmt) - 1)) - 1; }
+/* Asymmetric integer formats use codes 0..L with L = 2^b - 1. */
+static int asym_levels(int fmt) { return (1 << code_bits(fmt)) - 1; }
+
+size_t qro_encoded_bytes(int fmt, size_t n) {
+  if (fmt == QRO_FP) return n * 2;
+  if (!is_quantized(fmt)) return 0;
+  size_t nb = (n + QRO_BLOCK - 1) / QRO_BLOCK;
+  size_t cb = (size_t)QRO_BLOCK * (size_t)code_bits(fmt) / 8;
+  return nb * (cb + 2 + (is_asym(fmt) ? 2 : 0));
+}
+
+static float widen(int dtype, uint16_t v) {
+  return dtype == QRO_F16 ? qro_f16_to_f32(v) : qro_bf16_to_f32(v);
+}
+static uint16_t narrow(int dtype, float v) { /* d(v) */
+  return dtype == QRO_F16 ? qro_f32_to_f16(v) : qro_f32_to_bf16(v);
+}
+
+/* One encoded block: codes as integers, plus scale and zero-point both as the
+ * fp16 bit pattern that is stored and as its binary32 value. */
+typedef struct {
+  int q[QRO_BLOCK];
+  uint16_t s_bits, z_bits;
+  float s, z;
+} block_code;
+
+/* Encode the first cnt (1..32) values of x; pad codes (cnt..31) are 0.
+ *
+ * Symmetric Q8/Q6/Q4 (int8/int6/int4 symmetric of [P2]; Q8/Q6/Q4 of [P1]):
+ *   a = max |x_i|;  s = h(a / Qmax);
+ *   s == 0: every code 0;
+ *   else inv = 1 / s and q_i = clamp(rne(x_i * inv), -Qmax, Qmax).
+ * Asymmetric Q8a/Q4a (int8/int4 asymmetric of [P2]):
+ *   m = min x_i, M = max x_i;  s = h((M - m) / L);  z = h(m);
+ *   s == 0: every code 0;
+ *   else inv = 1 / s and q_i = clamp(rne((x_i - z) * inv), 0, L).
+ * FP8 (the "2stage f8" of [P1]; OCP e4m3fn codes with a per-block scale):
+ *   a = max |x_i|;  s = h(a / 448);
+ *   s == 0: every code 0;
+ *   else inv = 1 / s and q_i = e4m3fn(x_i * inv), rounded to nearest even and
+ *   saturated to +-448.
+ * The encoder divides by the rounded scale it stores, so the decoder
+ * multiplies by exactly the value the encoder assumed. */
+static void encode_block(int fmt, const float *x, int cnt, block_code *bc) {
+  memset(bc, 0, sizeof *bc);
+  if (is_asym(fmt)) {
+    float m = x[0], M = x[0];
+    for (int i = 1; i < cnt; ++i) {
+      if (x[i] < m) m = x[i];
+      if (x[i] > M) M = x[i];
+    }
+    const float L = (float)asym_levels(fmt);
+    float range = M - m;
+    float ratio = range / L;
+    bc->s_bits = qro_f32_to_f16_satfinite(ratio);
+    bc->z_bits = qro_f32_to_f16_satfinite(m);
+    bc->s = qro_f16_to_f32(bc->s_bits);
+    bc->z = qro_f16_to_f32(bc->z_bits);
+    if (bc->s == 0.0f) return;
+    float inv = 1.0f / bc->s;
+    for (int i = 0; i < cnt; ++i) {
+      float shifted = x[i] - bc->z;
+      float v = shifted * inv;
+      float r = rintf(v); /* round half to even (default rounding mode) */
+      if (r < 0.0f) r = 0.0f;
+      if (r > L) r = L;
+      bc->q[i] = (int)r;
+    }
+    return;
+  }
+  float a = 0.0f;
+  for (int i = 0; i < cnt; ++i) {
+    float ax = fabsf(x[i]);
+    if (ax > a) a = ax;
+  }
+  const float qmax = fmt == QRO_FP8 ? 448.0f : (float)sym_qmax(fmt);
+  float ratio = a / qmax;
+  bc->s_bits = qro_f32_to_f16_satfinite(ratio);
+  bc->s = qro_f16_to_f32(bc->s_bits);
+  if (bc->s == 0.0f) return;
+  float inv = 1.0f / bc->s;
+  for (int i = 0; i < cnt; ++i) {
+    float v = x[i] * inv;
+    if (fmt == QRO_FP8) {
+      bc->q[i] = qro_f32_to_e4m3_satfinite(v);
+    } else {
+      float r = rintf(v);
+      if (r < -qmax) r = -qmax;
+      if (r > qmax) r = qmax;
+      bc->q[i] = (int)r;
+    }
+  }
+}
+
+/* Decode one code: symmetric q*s, asymmetric q*s + z, FP8 e4m3(q)*s.
+ * (q*s is exact for every format: at most 8 by 11 significant bits.) */
+static float decode_value(int fmt, int q, float s, float z) {
+  if (is_asym(fmt)) {
+    float qs = (float)q * s;
+    return qs + z;
+  }
+  if (fmt == QRO_FP8) return qro_e4m3_to_f32((uint8_t)q) * s;
+  return (float)q * s;
+}
+
+/* Code i of a block occupies bits [b*i, b*i + b) of the block's little-endian
+ * bit stream (byte k holds stream bits 8k..8k+7, least significant first).
+ * Negative symmetric codes are stored in b-bit two's complement. */
+static void put_code(uint8_t *codes, int b, int i, int q) {
+  unsigned u = (unsigned)q & ((1u << b) - 1u);
+  for (int j = 0; j < b; ++j)
+    if ((u >> j) & 1u) codes[(b * i + j) / 8] |= (uint8_t)(1u << ((b * i + j) % 8));
+}
+
+static int get_code(const uint8_t *codes, int b, int i, int is_signed) {
+  unsigned u = 0;
+  for (int j = 0; j < b; ++j)
+    if ((codes[(b * i + j) / 8] >> ((b * i + j) % 8)) & 1u) u |= 1u << j;
+  if (is_signed && (u >> (b - 1)) & 1u) return (int)u - (1 << b);
+  return (int)u;
+}
+
+/* Encoded message layout (structure of arrays), nb = ceil(n / 32) blocks:
+ *   codes[nb][32*b/8] | scales[nb] (fp16, little-endian) | zps[nb] (asym) */
+static void store_block(int fmt, const block_code *bc, size_t blk, size_t nb, uint8_t *enc) {
+  int b = code_bits(fmt);
+  size_t cb = (size_t)QRO_BLOCK * (size_t)b / 8;
+  uint8_t *codes = enc + blk * cb;
+  memset(codes, 0, cb);
+  for (int i = 0; i < QRO_BLOCK; ++i) put_code(codes, b, i, bc->q[i]);
+  uint8_t *sc = enc + nb * cb + 2 * blk;
+  sc[0] = (uint8_t)(bc->s_bits & 0xFF);
+  sc[1] = (uint8_t)(bc->s_bits >> 8);
+  if (is_asym(fmt)) {
+    uint8_t *zp = enc + nb * cb + 2 * nb + 2 * blk;
+    zp[0] = (uint8_t)(bc->z_bits & 0xFF);
+    zp[1] = (uint8_t)(bc->z_bits >> 8);
+  }
+}
+
+static void load_block(int fmt, const uint8_t *enc, size_t blk, size_t nb, block_code *bc) {
+  int b = code_bits(fmt);
+  size_t cb = (size_t)QRO_BLOCK * (size_t)b / 8;
+  int is_signed = !is_asym(fmt) && fmt != QRO_FP8;
+  memset(bc, 0, sizeof *bc);
+  for (int i = 0; i < QRO_BLOCK; ++i) bc->q[i] = get_code(enc + blk * cb, b, i, is_signed);
+  const uint8_t *sc = enc + nb * cb + 2 * blk;
+  bc->s_bits = (uint16_t)(sc[0] | (sc[1] << 8));
+  bc->s = qro_f16_to_f32(bc->s_bits);
+  if (is_asym(fmt)) {
+    const uint8_t *zp = enc + nb * cb + 2 * nb + 2 * blk;
+    bc->z_bits = (uint16_t)(zp[0] | (zp[1] << 8));
+    bc->z = qro_f16_to_f32(bc->z_bits);
+  }
+}
+
+static int valid_format(int fmt) { return fmt == QRO_FP || is_quantized(fmt); }
+static int valid_dtype(int dt) { return dt == QRO_F16 || dt == QRO_BF16; }
+
+int qro_quantize(int dtype, int fmt, const uint16_t *in, size_t n, uint8_t *enc) {
+  if (!valid_dtype(dtype) || !valid_format(fmt) || (!in && n) || (!enc && n)) return -1;
+  if (fmt == QRO_FP) { /* passthrough: the encoded message is the values */
+    memcpy(enc, in, n * 2);
+    return 0;
+  }
+  size_t nb = (n + QRO_BLOCK - 1) / QRO_BLOCK;
+  for (size_t blk = 0; blk < nb; ++blk) {
+    size_t i0 = blk * QRO_BLOCK;
+    int cnt = (int)((n - i0) < QRO_BLOCK ? (n - i0) : QRO_BLOCK);
+    float x[QRO_BLOCK];
+    for (int i = 0; i < cnt; ++i) x[i] = widen(dtype, in[i0 + (size_t)i]);
+    block_code bc;
+    encode_block(fmt, x, cnt, &bc);
+    store_block(fmt, &bc, blk, nb, enc);
+  }
+  return 0;
+}
+
+int qro_dequantize(int dtype, int fmt, const uint8_t *enc, size_t n, uint16_t *out) {
+  if (!valid_dtype(dtype) || !valid_format(fmt) || (!enc && n) || (!out && n)) return -1;
+  if (fmt == QRO_FP) {
+    memcpy(out, enc, n * 2);
+    return 0;
+  }
+  size_t nb = (n + QRO_BLOCK - 1) / QRO_BLOCK;
+  for (size_t blk = 0; blk < nb; ++blk) {
+    size_t i0 = blk * QRO_BLOCK;
+    int cnt = (int)((n - i0) < QRO_BLOCK ? (n - i0) : QRO_BLOCK);
+    block_code bc;
+    load_block(fmt, enc, blk, nb, &bc);
+    for (int i = 0; i < cnt; ++i)
+      out[i0 + (size_t)i] = narrow(dtype, decode_value(fmt, bc.q[i], bc.s, bc.z));
+  }
+  return 0;
+}
+
+/* Emulated allreduce over W ranks, one 32-element block at a time (the codec
+ * is per block and the reduction is elementwise, so the result does not
+ * depend on how blocks are split among owning ranks).
+ *
+ *   1. x_r = the block of rank r, widened exactly to binary32.
+ *   2. Stage 1 (reduce-scatter, "2stage" of [P1], "two shot" of [P2]):
+ *      a quantized format sends every rank's block through the codec,
+ *      xhat_r = decode(encode(x_r)); FP passthrough sends x_r as is.
+ *      The quantized one-stage variant does the same (each rank reads every
+ *      other rank's encoded block, "one shot" of [P2]).
+ *   3. acc = xhat_0, then acc = acc + xhat_r for r = 1..W-1 (binary32, rank
+ *      order).
+ *   4. Stage 2 (all-gather), stages == 2 only: a quantized format encodes
+ *      acc itself and every rank decodes that, yhat = decode(encode(acc)),
+ *      and the encoded block is the wire payload; FP passthrough sends
+ *      d(acc), so yhat = d(acc) and the payload is d(acc).
+ *      stages == 1: yhat = acc.
+ *   5. out = d(yhat): the same on every rank, so one copy is produced. */
+int qro_allreduce(int W, int dtype, int fmt, int stages,
+                  const uint16_t *const *inputs, size_t n,
+                  uint16_t *out, uint8_t *wire) {
+  if (W < 1 || W > 8 || !valid_dtype(dtype) || !valid_format(fmt)) return -1;
+  if (stages != 1 && stages != 2) return -1;
+  if (n && (!inputs || !out)) return -1;
+  for (int r = 0; r < W && n; ++r)
+    if (!inputs[r]) return -1;
+  size_t nb = (n + QRO_BLOCK - 1) / QRO_BLOCK;
+  for (size_t blk = 0; blk < nb; ++blk) {
+    size_t i0 = blk * QRO_BLOCK;
+    int cnt = (int)((n - i0) < QRO_BLOCK ? (n - i0) : QRO_BLOCK);
+    float acc[QRO_BLOCK];
+    for (int r = 0; r < W; ++r) {
+      float x[QRO_BLOCK], xhat[QRO_BLOCK];
+      for (int i = 0; i < cnt; ++i) x[i] = widen(dtype, inputs[r][i0 + (size_t)i]);
+      if (is_quantized(fmt)) {
+        block_code bc;
+        encode_block(fmt, x, cnt, &bc);
+        for (int i = 0; i < cnt; ++i) xhat[i] = decode_value(fmt, bc.q[i], bc.s, bc.z);
+      } else {
+        for (int i = 0; i < cnt; ++i) xhat[i] = x[i];
+      }
+      for (int i = 0; i < cnt; ++i) acc[i] = (r == 0) ? xhat[i] : acc[i] + xhat[i];
+    }
+    for (int i = 0; i < cnt; ++i) {
+      /* stage 1 only: yhat = acc; overwritten below for stage 2 */
+      out[i0 + (size_t)i] = narrow(dtype, acc[i]);
+    }
+    if (stages == 2) {
+      if (is_quantized(fmt)) {
+        block_code bc;
+        encode_block(fmt, acc, cnt, &bc);
+        if (wire) store_block(fmt, &bc, blk, nb, wire);
+        for (int i = 0; i < cnt; ++i)
+          out[i0 + (size_t)i] = narrow(dtype, decode_value(fmt, bc.q[i], bc.s, bc.z));
+      } else {
+        for (int i = 0; i < cnt; ++i) {
+          uint16_t v = narrow(dtype, acc[i]);
+          if (wire) {
+            wire[2 * (i0 + (size_t)i)] = (uint8_t)(v & 0xFF);
+            wire[2 * (i0 + (size_t)i) + 1] = (uint8_t)(v >> 8);
+          }
+          /* yhat = widen(d(acc)); out = d(yhat) = d(acc) */
+          out[i0 + (size_t)i] = narrow(dtype, widen(dtype, v));
+        }
+      }
+    }
+  }
+  return 0;
+}
