@@ -1,0 +1,506 @@
+#!/usr/bin/env python3
+"""Benchmark of the emulated quick-allreduce data path on one GB300 (or N
+independent replicas, one per GPU).
+
+One step = one pass of the whole hot path over the tp2 workload of the vLLM
+PR #18473 timing table at its largest size: W=2 emulated ranks, fp16,
+64 MiB per rank, N(0,1), in the table's six kernels -- FP one-stage, FP
+two-stage, FP8, Q8, Q6 and Q4 two-stage (every two-stage call also writes
+its stage-2 payload).  Inputs are resident in HBM; L2 is flushed (a write
+of at least twice its size) before every timed call, outside the timed
+events.
+
+metric: GB/s per rank-message = sum of per-rank message bytes (n*2) over
+the calls / sum of their device times (CUDA events on the launching
+stream).  The JSON line also carries the HBM roofline of the fused
+two-stage quantized kernel, the oracle's CPU rate on a bounded sample, an
+end-to-end rate through the C ABI with host buffers, a size sweep, and the
+other workloads.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 is launched with torchrun; each rank runs the same workload on its
+own GPU (replicas: the emulated path has no inter-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from quantized_allreduce_codec_gb300.inputs import (BF16, F16, FORMAT_NAMES, FP, FP8, Q4,  # noqa: E402
+                                                    Q4A, Q6, Q8, Q8A, sweep_sizes_bytes,
+                                                    sweep_workload, workloads)
+
+METRIC = "emulated quick-allreduce GB/s per rank-message and % of HBM roofline, 1×GB300"
+STEP_CALLS = [(FP, 1), (FP, 2), (FP8, 2), (Q8, 2), (Q6, 2), (Q4, 2)]  # the tp2 table's kernels
+BENCH_BYTES = 64 << 20
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+CODE_BITS = {Q8: 8, Q6: 6, Q4: 4, FP8: 8, Q8A: 8, Q4A: 4}
+
+
+def encoded_bytes(fmt: int, n: int) -> int:
+    if fmt == FP:
+        return 2 * n
+    nb = (n + 31) // 32
+    return nb * (32 * CODE_BITS[fmt] // 8 + (4 if fmt in (Q8A, Q4A) else 2))
+
+
+def bytes_alg(W: int, n: int, fmt: int, stages: int, wire: bool) -> int:
+    """Algorithmic bytes of one emulated allreduce: read W messages, write the
+    output, plus the stage-2 payload when it is written."""
+    b = W * n * 2 + n * 2
+    if stages == 2 and wire:
+        b += encoded_bytes(fmt, n)
+    return b
+
+
+def step_name(fmt: int, stages: int) -> str:
+    return f"{FORMAT_NAMES[fmt]}-{stages}stage"
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas) -- host logic, tested with gloo on CPU
+# ----------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def dist_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_bytes: float, max_seconds: float, world: int) -> float:
+    """Whole-job GB/s: every rank moves per_rank_bytes in at most max_seconds."""
+    return world * per_rank_bytes / max_seconds / 1e9
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str, interval_ms: int = 50):
+        self.index, self.interval = index, interval_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def smi_device_id(props, local: int) -> str:
+    """nvidia-smi -i selector of this process's GPU (UUID, else PCI bus id,
+    else the CUDA index)."""
+    uuid = getattr(props, "uuid", None)
+    if uuid:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    bus = getattr(props, "pci_bus_id", None)
+    if bus is not None:
+        return f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+    return str(local)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel_source: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (matched by hash); else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "qr_pipeline_traffic.txt")
+    try:
+        fields = dict(ln.split("=", 1) for ln in open(path).read().split() if "=" in ln)
+        src = open(kernel_source, "rb").read()
+        if fields.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return fields
+    except OSError:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import quantized_allreduce_codec_gb300 as qr
+    from quantized_allreduce_codec_gb300 import build as qr_build
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    if rank == 0 or not os.path.exists(qr.LIB_PATH):
+        qr_build.build()
+    dist_barrier()
+    qr.lib()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
+    flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    wl = sweep_workload(BENCH_BYTES)
+    n, W = wl.n, wl.W
+    host = wl.inputs()
+    ins = [torch.from_numpy(x.view(np.int16)).to(dev) for x in host]
+    out = torch.empty(n, dtype=torch.int16, device=dev)
+    wires = {f: torch.empty(encoded_bytes(f, n), dtype=torch.uint8, device=dev) for f, _ in STEP_CALLS}
+
+    def call(fmt, stages, inputs=ins, nn=n, o=out):
+        qr.qr_allreduce_emulated(len(inputs), wl.dtype, fmt, stages, inputs, nn, o,
+                                 wires[fmt] if stages == 2 else None, stream)
+
+    # warm-up (also first-call set-up of every instantiation used)
+    for _ in range(args.warmup):
+        for fmt, st in STEP_CALLS:
+            flush()
+            call(fmt, st)
+    torch.cuda.synchronize()
+    if qr.qr_device_error() != 0:
+        raise RuntimeError("kernel wait-limit flag raised during warm-up")
+
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in STEP_CALLS] for _ in range(K)]
+    sampler = ClockSampler(smi_device_id(props, local))
+    dist_barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.2)
+    wall0 = time.perf_counter()
+    for k in range(K):
+        for j, (fmt, st) in enumerate(STEP_CALLS):
+            flush()
+            ev[k][j][0].record(stream)
+            call(fmt, st)
+            ev[k][j][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    dist_barrier()
+    clocks = sampler.stop()
+    if qr.qr_device_error() != 0:
+        raise RuntimeError("kernel wait-limit flag raised in the timed region")
+
+    times = np.array([[a.elapsed_time(b) * 1e-3 for a, b in row] for row in ev])  # seconds [K, calls]
+    per_call = times.sum(axis=0) / K
+    my_total = float(times.sum())
+    max_total = dist_max(my_total, dev)
+    step_bytes = sum(n * 2 for _ in STEP_CALLS)
+    value = aggregate(K * step_bytes, max_total, world)
+
+    peak, peak_kind = read_peaks()
+    per_format = {}
+    q_bytes = q_time = 0.0
+    for j, (fmt, st) in enumerate(STEP_CALLS):
+        b = bytes_alg(W, n, fmt, st, st == 2)
+        t = float(np.median(times[:, j]))
+        per_format[step_name(fmt, st)] = {
+            "us_median": round(t * 1e6, 2), "us_min": round(float(times[:, j].min()) * 1e6, 2),
+            "algbw_GBps": round(n * 2 / t / 1e9, 1), "hbm_GBps": round(b / t / 1e9, 1),
+            "frac_of_measured_peak": round(b / t / 1e9 / peak, 3)}
+        if fmt != FP:
+            q_bytes += b * K
+            q_time += float(times[:, j].sum())
+    achieved = q_bytes / q_time / 1e9
+    traffic = recorded_traffic(os.path.join(ROOT, "quantized_allreduce_codec_gb300", "csrc",
+                                            "qr_device.cuh"))
+    roofline = {"kernel": "qr_pipeline_kernel (fused two-stage, quantized formats FP8/Q8/Q6/Q4, fp16, W=2)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "frac_of_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 4),
+                "traffic": (float(traffic["bytes_per_launch"]) if traffic else None),
+                "algorithmic_bytes_per_launch": round(q_bytes / (4 * K)),
+                "traffic_note": (traffic.get("note") if traffic else
+                                 "no ncu capture of the current kernel source")}
+
+    # ---------------- end to end through the C ABI, host buffers ----------------
+    Ke = max(1, min(args.steps, args.e2e_steps))
+    pin_in = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in host]
+    pin_out = torch.empty(n, dtype=torch.int16).pin_memory()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for warm in (True, False):
+        torch.cuda.synchronize()
+        dist_barrier()
+        e_start.record(stream)
+        for _ in range(1 if warm else Ke):
+            for fmt, st in STEP_CALLS:
+                for d, h in zip(ins, pin_in):
+                    d.copy_(h, non_blocking=True)
+                call(fmt, st)
+                pin_out.copy_(out, non_blocking=True)
+        e_end.record(stream)
+        torch.cuda.synchronize()
+    e2e_t = dist_max(e_start.elapsed_time(e_end) * 1e-3, dev)
+    e2e = {"value": round(aggregate(Ke * step_bytes, e2e_t, world), 2), "unit": "GB/s",
+           "h2d_bytes_per_step": sum(W * n * 2 for _ in STEP_CALLS),
+           "d2h_bytes_per_step": sum(n * 2 for _ in STEP_CALLS), "steps": Ke,
+           "note": "pinned host inputs copied in and the output copied back around every call"}
+    del pin_in, pin_out
+
+    # ---------------- size sweep (tp2 table sizes) ----------------
+    sweep = {}
+    if not args.no_extras:
+        for size in sweep_sizes_bytes():
+            nn = size // 2
+            sub = [t[:nn] for t in ins]
+            row = {}
+            for fmt, st in STEP_CALLS:
+                ts = []
+                for it in range(args.warmup + args.sweep_iters):
+                    flush()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    call(fmt, st, sub, nn, out)
+                    b.record(stream)
+                    if it >= args.warmup:
+                        ts.append((a, b))
+                torch.cuda.synchronize()
+                t = float(np.median([x.elapsed_time(y) for x, y in ts])) * 1e-3
+                row[step_name(fmt, st)] = {"us": round(t * 1e6, 2),
+                                           "hbm_frac": round(bytes_alg(W, nn, fmt, st, st == 2) / t / 1e9 / peak, 3)}
+            sweep[str(size)] = row
+
+    # ---------------- the other workloads ----------------
+    extra = {}
+    if not args.no_extras:
+        del ins
+        torch.cuda.empty_cache()
+        for key in (3, 4, 5):
+            w = workloads()[key]
+            dins = [torch.from_numpy(w.rank_bits(r).view(np.int16)).to(dev) for r in range(w.W)]
+            o = torch.empty(w.n, dtype=torch.int16, device=dev)
+            res = {}
+            for fmt in w.formats:
+                wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
+                for st in w.stages:
+                    ts = []
+                    for it in range(args.warmup + args.sweep_iters):
+                        flush()
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        qr.qr_allreduce_emulated(w.W, w.dtype, fmt, st, dins, w.n, o,
+                                                 wire if st == 2 else None, stream)
+                        b.record(stream)
+                        if it >= args.warmup:
+                            ts.append((a, b))
+                    torch.cuda.synchronize()
+                    t = float(np.median([x.elapsed_time(y) for x, y in ts])) * 1e-3
+                    ba = bytes_alg(w.W, w.n, fmt, st, st == 2)
+                    res[step_name(fmt, st)] = {"us": round(t * 1e6, 1),
+                                               "algbw_GBps": round(w.n * 2 / t / 1e9, 1),
+                                               "hbm_GBps": round(ba / t / 1e9, 1),
+                                               "hbm_frac": round(ba / t / 1e9 / peak, 3)}
+                del wire
+            extra[w.name] = res
+            del dins, o
+            torch.cuda.empty_cache()
+        if qr.qr_device_error() != 0:
+            raise RuntimeError("kernel wait-limit flag raised in the extras")
+
+    # ---------------- CPU baseline: the oracle on a bounded sample ----------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(host, wl.dtype, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(max_total / K * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "tp2 table, largest size: W=2 emulated ranks, fp16, 64 MiB "
+                                   "(33554432 elements) per rank, N(0,1) seed 2000+r; one step = "
+                                   "FP 1-stage, FP 2-stage, FP8, Q8, Q6, Q4 2-stage (payload written)",
+                       "W": W, "per_rank_bytes": n * 2, "calls_per_step": len(STEP_CALLS),
+                       "l2": f"flushed before every timed call ({flush_buf.numel() * 4 >> 20} MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, W ranks emulated in HBM"},
+            "roofline": roofline, "per_format": per_format,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": K * len(STEP_CALLS),
+            "clocks": clocks, "wall_ms_per_step_incl_flush": round(wall / K * 1e3, 3),
+            "sweep_W2_fp16": sweep, "workloads": extra,
+        }
+        print(json.dumps(line), flush=True)
+    dist_barrier()
+
+
+def cpu_baseline(host, dtype, seconds: float) -> dict:
+    """The oracle, single-threaded, on a prefix of the bench workload sized to
+    about `seconds` of CPU time, over the step's six calls."""
+    import oracle
+    oracle.build()
+
+    def run(m):
+        t0 = time.perf_counter()
+        for fmt, st in STEP_CALLS:
+            oracle.allreduce(dtype, fmt, st, [x[:m] for x in host])
+        return time.perf_counter() - t0
+
+    probe = 1 << 15
+    tp = run(probe)
+    m = int(min(host[0].size, max(probe, probe * seconds / max(tp, 1e-6))))
+    m -= m % 32
+    t = run(m)
+    return {"value": round(len(STEP_CALLS) * m * 2 / t / 1e9, 5), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"first {m} elements ({m * 2 / 2**20:.1f} MiB) of each rank's message, "
+                      f"all {len(STEP_CALLS)} calls of one step, {t:.1f} s single-threaded"}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the oracle, timed on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = sweep_workload(BENCH_BYTES)
+    m = args.ref_elems
+    host = [wl.rank_bits(r)[:m] for r in range(wl.W)]
+    for _ in range(args.warmup):
+        for fmt, st in STEP_CALLS:
+            oracle.allreduce(wl.dtype, fmt, st, host)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for fmt, st in STEP_CALLS:
+            oracle.allreduce(wl.dtype, fmt, st, host)
+    t = time.perf_counter() - t0
+    value = args.steps * len(STEP_CALLS) * m * 2 / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "tp2 table, largest size: W=2 emulated ranks, fp16, 64 MiB per rank, "
+                               "N(0,1); one step = FP 1-stage, FP 2-stage, FP8, Q8, Q6, Q4 2-stage; "
+                               f"each step runs the CPU oracle on the first {m} elements of each rank",
+                   "W": wl.W, "per_rank_bytes": wl.n * 2},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(value, 6), "unit": "GB/s",
+                         "sample": f"first {m} elements of each rank's message per call"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the reference arm is the repository's CPU oracle (no reference implementation ships "
+                "with the source pages)",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-elems", type=int, default=1 << 18)
+    ap.add_argument("--no-extras", action="store_true", help="skip the size sweep and other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,156 @@
+/*
+ * qr.h -- C ABI of libqr.so, a GB300 (sm_103a) implementation of the
+ * quick-allreduce data path: a low-granularity block quantize/dequantize
+ * codec and a one- and two-stage allreduce in which the W tensor-parallel
+ * ranks are emulated as W fp16/bf16 buffers in one GPU's memory.
+ *
+ * Sources (web pages):
+ *   vLLM PR #18473, "Integrate quick allreduce and select the best allreduce
+ *     implementation": opening description (1stage f16; 2stage f16, fp8,
+ *     Q8, Q6, Q4) and the tp2 kernel timing table.
+ *   vLLM PR #16804, "Add quickreduce as alternative to custom allreduce":
+ *     opening description (int4/int8, symmetric and asymmetric) and review
+ *     discussion (one shot for small buffers, two shot for larger ones).
+ *   vLLM API docs, "vllm.distributed.device_communicators.quick_all_reduce":
+ *     QuickReduceRegime (FP=0, INT8=1, INT6=2, INT4=3), _SUPPORTED_DTYPES
+ *     (float16, bfloat16), _SUPPORTED_WORLD_SIZES (2, 4, 8),
+ *     should_quick_allreduce (input byte size a multiple of 16) and
+ *     quick_all_reduce (out-of-place; ops.qr_all_reduce(..., level, ...)).
+ *
+ * Codec.  A message of n elements is cut into nb = ceil(n/32) blocks of 32.
+ * Each block gets an fp16 scale s (and, for the asymmetric formats, an fp16
+ * zero-point z) and 32 b-bit codes:
+ *   symmetric  Q8/Q6/Q4 (b = 8/6/4): s = h(max|x| / Qmax), Qmax = 2^(b-1)-1,
+ *              q = clamp(rne(x * (1/s)), -Qmax, Qmax), decoded as q*s;
+ *   asymmetric Q8A/Q4A (b = 8/4):    s = h((max x - min x) / (2^b - 1)),
+ *              z = h(min x), q = clamp(rne((x - z) * (1/s)), 0, 2^b - 1),
+ *              decoded as q*s + z;
+ *   FP8 (e4m3fn codes):              s = h(max|x| / 448),
+ *              q = e4m3(x * (1/s)) rounded to nearest even and saturated,
+ *              decoded as e4m3(q)*s;
+ *   FP:        passthrough, no codes.
+ * h() rounds binary32 to fp16 to nearest even and saturates at +-65504; all
+ * arithmetic is binary32, round-to-nearest-even; a block whose scale
+ * rounds to 0 gets all-zero codes.  The final block of a message whose n is
+ * not a multiple of 32 takes its statistics over its valid elements; its
+ * pad codes are 0.
+ *
+ * Encoded message layout (for qr_quantize's enc and qr_allreduce_emulated's
+ * wire), structure of arrays:
+ *   codes [nb][32*b/8 bytes]   code i of a block occupies bits [b*i, b*i+b)
+ *                              of the block's little-endian bit stream;
+ *                              symmetric codes are b-bit two's complement
+ *   scales[nb]  fp16
+ *   zps   [nb]  fp16           (asymmetric formats only)
+ * For QR_FP the encoded message is the n values themselves (n*2 bytes).
+ *
+ * Conventions for every call:
+ *   - All buffers are caller-owned DEVICE memory on the current device, and
+ *     must be 16-byte aligned.  The library allocates nothing.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  QR_OK means the launch was accepted; a failed launch
+ *     returns QR_ERR_CUDA.  Nothing synchronises the device.
+ *   - n == 0 is a valid empty message: nothing is launched and pointers may
+ *     be NULL.
+ *   - Errors are reported by the return value only; no call aborts or
+ *     prints.
+ */
+#ifndef QR_H
+#define QR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Message dtypes (_SUPPORTED_DTYPES on the quick_all_reduce API page). */
+typedef enum { QR_F16 = 0, QR_BF16 = 1 } qr_dtype;
+
+/* Formats.  0..3 are QuickReduceRegime's values (FP, INT8, INT6, INT4) from
+ * the quick_all_reduce API page; 4 is the "2stage f8" format of vLLM PR
+ * #18473; 5 and 6 are the asymmetric int8/int4 formats of vLLM PR #16804. */
+typedef enum {
+  QR_FP = 0, QR_Q8 = 1, QR_Q6 = 2, QR_Q4 = 3,
+  QR_FP8 = 4, QR_Q8_ASYM = 5, QR_Q4_ASYM = 6
+} qr_format;
+
+typedef enum {
+  QR_OK = 0,
+  QR_ERR_NULL = 1,    /* a required pointer is NULL (n > 0)                   */
+  QR_ERR_DTYPE = 2,   /* dtype is not fp16 or bf16                            */
+  QR_ERR_FORMAT = 3,  /* unknown format                                       */
+  QR_ERR_WORLD = 4,   /* W not in {1, 2, 4, 8}                                */
+  QR_ERR_STAGES = 5,  /* stages not in {1, 2}, or a wire buffer with stages 1 */
+  QR_ERR_SIZE = 6,    /* n*2 bytes is not a multiple of 16, or n too large    */
+  QR_ERR_ALIGN = 7,   /* a pointer is not 16-byte aligned                     */
+  QR_ERR_OVERLAP = 8, /* an output buffer overlaps an input or another output */
+  QR_ERR_CUDA = 9,    /* the CUDA runtime reported an error                   */
+  QR_ERR_DEVICE = 10  /* a kernel gave up waiting (see qr_device_error)       */
+} qr_status;
+
+/* Largest n accepted (elements per message): 2^36. */
+#define QR_MAX_ELEMS ((uint64_t)1 << 36)
+
+/* Bytes of one encoded message of n elements in format fmt:
+ * nb*(32*b/8 + 2) for symmetric and FP8, nb*(32*b/8 + 4) for asymmetric,
+ * n*2 for QR_FP; 0 for an unknown format.  Host only, no CUDA call. */
+size_t qr_encoded_bytes(qr_format fmt, size_t n);
+
+/* Encode one message (the codec's quantize step; the sender side of
+ * "2stage ... Q8/Q6/Q4" in vLLM PR #18473).
+ *   in   device, n values of dtype dt, 16-byte aligned, read only
+ *   enc  device, qr_encoded_bytes(fmt, n) bytes, 16-byte aligned, written
+ * enc must not overlap in. */
+qr_status qr_quantize(qr_dtype dt, qr_format fmt, const void *in, size_t n,
+                      void *enc, void *stream);
+
+/* Decode one encoded message back to n values of dtype dt (the receiver
+ * side of the codec).
+ *   enc  device, qr_encoded_bytes(fmt, n) bytes, 16-byte aligned, read only
+ *   out  device, n values of dtype dt, 16-byte aligned, written
+ * out must not overlap enc. */
+qr_status qr_dequantize(qr_dtype dt, qr_format fmt, const void *enc, size_t n,
+                        void *out, void *stream);
+
+/* Emulated quick allreduce of W messages (quick_all_reduce on the API page:
+ * out-of-place, one call per allreduce; "1stage" and "2stage" of vLLM PR
+ * #18473).  For every 32-element block, in this order:
+ *   1. each rank's block is widened to binary32;
+ *   2. stage 1 (reduce-scatter): for a quantized format every rank's block
+ *      goes through the codec, xhat_r = decode(encode(x_r)); FP sends x_r;
+ *   3. acc = xhat_0 + xhat_1 + ... + xhat_{W-1}, binary32, in rank order;
+ *   4. stages == 2 (all-gather): a quantized format requantizes acc and
+ *      every rank decodes the requantized block; FP rounds acc to dtype;
+ *      stages == 1: acc is used as is (the one-shot variant: every rank
+ *      reads every other rank's stage-1 data);
+ *   5. out = the result rounded to dtype (round to nearest even).
+ * The result is identical on all emulated ranks, so one copy is written.
+ *   W       number of emulated ranks, 1, 2, 4 or 8 (1 = identity check)
+ *   inputs  HOST array of W device pointers, each n values of dtype dt,
+ *           16-byte aligned, read only (the array is read during the call)
+ *   out     device, n values of dtype dt, 16-byte aligned, written
+ *   wire    optional device buffer of qr_encoded_bytes(fmt, n) bytes that
+ *           receives the stage-2 payload (the requantized blocks; for QR_FP
+ *           the dtype-rounded sums); NULL to skip; must be NULL when
+ *           stages == 1
+ * out and wire must not overlap any input or each other. */
+qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages,
+                                const void *const *inputs, size_t n,
+                                void *out, void *wire, void *stream);
+
+/* A short English description of a status code (static storage). */
+const char *qr_status_string(qr_status st);
+
+/* Kernels never wait forever: a pipeline wait that exceeds its time limit
+ * sets a flag in device memory and the kernel returns early.  This call
+ * synchronises the current device, copies the flags to *flags (0 = none
+ * raised) and clears them when clear != 0.  Returns QR_ERR_DEVICE when a
+ * flag was raised, QR_OK otherwise, QR_ERR_CUDA on a CUDA error. */
+qr_status qr_device_error(unsigned int *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QR_H */

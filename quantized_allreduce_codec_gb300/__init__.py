@@ -1,0 +1,141 @@
+"""GB300 quick-allreduce codec: thin Python binding of libqr.so (include/qr.h).
+
+Argument marshalling only: every step of the data path runs in the CUDA
+kernels of libqr.so.  If the library has not been built this module raises
+on first use; there is no fallback.  Build with
+``python -m quantized_allreduce_codec_gb300.build``.
+
+Functions take torch tensors (device memory, contiguous) or raw integer
+device addresses; ``stream`` defaults to torch's current CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+F16, BF16 = 0, 1
+QR_FP, QR_Q8, QR_Q6, QR_Q4, QR_FP8, QR_Q8_ASYM, QR_Q4_ASYM = 0, 1, 2, 3, 4, 5, 6
+FORMATS = {"FP": QR_FP, "Q8": QR_Q8, "Q6": QR_Q6, "Q4": QR_Q4, "FP8": QR_FP8,
+           "Q8A": QR_Q8_ASYM, "Q4A": QR_Q4_ASYM}
+STATUS = ["QR_OK", "QR_ERR_NULL", "QR_ERR_DTYPE", "QR_ERR_FORMAT", "QR_ERR_WORLD",
+          "QR_ERR_STAGES", "QR_ERR_SIZE", "QR_ERR_ALIGN", "QR_ERR_OVERLAP", "QR_ERR_CUDA",
+          "QR_ERR_DEVICE"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqr.so")
+EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
+           "qr_status_string", "qr_device_error")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class QRError(RuntimeError):
+    """A libqr call returned a status other than QR_OK."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        name = STATUS[status] if 0 <= status < len(STATUS) else str(status)
+        super().__init__(f"{what}: {name} ({qr_status_string(status)})")
+
+
+def lib():
+    """The loaded libqr.so (ctypes.CDLL); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(f"libqr.so not built ({LIB_PATH}); run "
+                                       "python -m quantized_allreduce_codec_gb300.build")
+                L = ctypes.CDLL(LIB_PATH)
+                vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+                L.qr_encoded_bytes.restype = sz
+                L.qr_encoded_bytes.argtypes = [i, sz]
+                L.qr_quantize.restype = i
+                L.qr_quantize.argtypes = [i, i, vp, sz, vp, vp]
+                L.qr_dequantize.restype = i
+                L.qr_dequantize.argtypes = [i, i, vp, sz, vp, vp]
+                L.qr_allreduce_emulated.restype = i
+                L.qr_allreduce_emulated.argtypes = [i, i, i, i, vp, sz, vp, vp, vp]
+                L.qr_status_string.restype = ctypes.c_char_p
+                L.qr_status_string.argtypes = [i]
+                L.qr_device_error.restype = i
+                L.qr_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
+                _lib = L
+    return _lib
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise QRError(st, what)
+
+
+def _dtype_code(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    import torch
+    if dtype == torch.float16:
+        return F16
+    if dtype == torch.bfloat16:
+        return BF16
+    raise ValueError(f"unsupported dtype {dtype}")
+
+
+def qr_status_string(status: int) -> str:
+    return lib().qr_status_string(status).decode()
+
+
+def qr_encoded_bytes(fmt: int, n: int) -> int:
+    return int(lib().qr_encoded_bytes(fmt, n))
+
+
+def qr_quantize(dtype, fmt: int, inp, n: int, enc, stream=None) -> None:
+    """Encode n values of `inp` into `enc` (qr_encoded_bytes(fmt, n) bytes)."""
+    _check(lib().qr_quantize(_dtype_code(dtype), fmt, _addr(inp), n, _addr(enc), _stream(stream)),
+           "qr_quantize")
+
+
+def qr_dequantize(dtype, fmt: int, enc, n: int, out, stream=None) -> None:
+    """Decode an encoded message into n values of `out`."""
+    _check(lib().qr_dequantize(_dtype_code(dtype), fmt, _addr(enc), n, _addr(out), _stream(stream)),
+           "qr_dequantize")
+
+
+def qr_allreduce_emulated(W: int, dtype, fmt: int, stages: int, inputs, n: int, out,
+                          wire=None, stream=None) -> None:
+    """Emulated allreduce of W rank messages (list of W tensors / addresses)."""
+    ptrs = (ctypes.c_void_p * max(len(inputs), 1))(*[_addr(x) for x in inputs])
+    _check(lib().qr_allreduce_emulated(W, _dtype_code(dtype), fmt, stages,
+                                       ctypes.cast(ptrs, ctypes.c_void_p) if inputs else None, n,
+                                       _addr(out), _addr(wire), _stream(stream)),
+           "qr_allreduce_emulated")
+
+
+def qr_device_error(clear: bool = True) -> int:
+    """Synchronise and return the kernels' wait-limit flags (0 = none)."""
+    flags = ctypes.c_uint(0)
+    st = lib().qr_device_error(ctypes.byref(flags), 1 if clear else 0)
+    if st not in (0, 10):
+        raise QRError(st, "qr_device_error")
+    return int(flags.value)

@@ -1,0 +1,234 @@
+// qr_api.cu -- the C ABI of libqr.so (declared in include/qr.h): argument
+// validation, encoded-buffer layout, dispatch to the per-format launchers.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "qr.h"
+#include "qr_launch.h"
+
+namespace qr {
+
+__device__ unsigned g_qr_error_flags;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int code_bits(int fmt) {
+  switch (fmt) {
+    case FMT_Q8: case FMT_FP8: case FMT_Q8A: return 8;
+    case FMT_Q6: return 6;
+    case FMT_Q4: case FMT_Q4A: return 4;
+    default: return 0;
+  }
+}
+bool is_asym(int fmt) { return fmt == FMT_Q8A || fmt == FMT_Q4A; }
+bool valid_format(int fmt) { return fmt >= FMT_FP && fmt <= FMT_Q4A; }
+bool valid_dtype(int dt) { return dt == DT_F16 || dt == DT_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na && nb && x < y + nb && y < x + na;
+}
+
+qr_status check_size(size_t n) {
+  if (n > QR_MAX_ELEMS) return QR_ERR_SIZE;
+  if ((n * 2) % 16 != 0) return QR_ERR_SIZE;  // byte size a multiple of 16
+  return QR_OK;
+}
+
+qr_status to_status(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_CUDA; }
+
+cudaError_t dispatch_pipeline(int fmt, int dt, int mode, const PipeParams& p, cudaStream_t s) {
+  switch (fmt) {
+    case 0: return launch_pipeline_fmt_0(dt, mode, p, s);
+    case 1: return launch_pipeline_fmt_1(dt, mode, p, s);
+    case 2: return launch_pipeline_fmt_2(dt, mode, p, s);
+    case 3: return launch_pipeline_fmt_3(dt, mode, p, s);
+    case 4: return launch_pipeline_fmt_4(dt, mode, p, s);
+    case 5: return launch_pipeline_fmt_5(dt, mode, p, s);
+    case 6: return launch_pipeline_fmt_6(dt, mode, p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t dispatch_decode(int fmt, int dt, const DecodeParams& p, cudaStream_t s) {
+  switch (fmt) {
+    case 0: return launch_decode_fmt_0(dt, p, s);
+    case 1: return launch_decode_fmt_1(dt, p, s);
+    case 2: return launch_decode_fmt_2(dt, p, s);
+    case 3: return launch_decode_fmt_3(dt, p, s);
+    case 4: return launch_decode_fmt_4(dt, p, s);
+    case 5: return launch_decode_fmt_5(dt, p, s);
+    case 6: return launch_decode_fmt_6(dt, p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Encoded layout: codes[nb][cb] | scales[nb] | zps[nb] (asymmetric only).
+void encoded_regions(int fmt, size_t n, void* base, uint8_t** codes, uint16_t** scales, uint16_t** zps,
+                     uint16_t** fp_values) {
+  *codes = nullptr;
+  *scales = *zps = *fp_values = nullptr;
+  if (!base) return;
+  if (fmt == FMT_FP) {
+    *fp_values = static_cast<uint16_t*>(base);
+    return;
+  }
+  const size_t nb = (n + 31) / 32;
+  const size_t cb = 32 * static_cast<size_t>(code_bits(fmt)) / 8;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  *codes = b;
+  *scales = reinterpret_cast<uint16_t*>(b + nb * cb);
+  if (is_asym(fmt)) *zps = reinterpret_cast<uint16_t*>(b + nb * cb + 2 * nb);
+}
+
+}  // namespace
+
+unsigned* device_error_word() {
+  static unsigned* addr[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qr_error_flags) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace qr
+
+using namespace qr;
+
+extern "C" {
+
+size_t qr_encoded_bytes(qr_format fmt, size_t n) {
+  const int f = static_cast<int>(fmt);
+  if (!valid_format(f)) return 0;
+  if (f == FMT_FP) return n * 2;
+  const size_t nb = (n + 31) / 32;
+  return nb * (32 * static_cast<size_t>(code_bits(f)) / 8 + 2 + (is_asym(f) ? 2 : 0));
+}
+
+const char* qr_status_string(qr_status st) {
+  switch (st) {
+    case QR_OK: return "ok";
+    case QR_ERR_NULL: return "a required pointer is NULL";
+    case QR_ERR_DTYPE: return "dtype must be fp16 or bf16";
+    case QR_ERR_FORMAT: return "unknown format";
+    case QR_ERR_WORLD: return "world size must be 1, 2, 4 or 8";
+    case QR_ERR_STAGES: return "stages must be 1 or 2 (and wire must be NULL for 1)";
+    case QR_ERR_SIZE: return "message byte size must be a multiple of 16 (and n <= 2^36)";
+    case QR_ERR_ALIGN: return "buffers must be 16-byte aligned";
+    case QR_ERR_OVERLAP: return "an output buffer overlaps an input or another output";
+    case QR_ERR_CUDA: return "CUDA runtime error";
+    case QR_ERR_DEVICE: return "a kernel gave up waiting on its pipeline";
+    default: return "unknown status";
+  }
+}
+
+qr_status qr_quantize(qr_dtype dt, qr_format fmt, const void* in, size_t n, void* enc, void* stream) {
+  const int f = static_cast<int>(fmt), d = static_cast<int>(dt);
+  if (n && (!in || !enc)) return QR_ERR_NULL;
+  if (!valid_dtype(d)) return QR_ERR_DTYPE;
+  if (!valid_format(f)) return QR_ERR_FORMAT;
+  qr_status st = check_size(n);
+  if (st != QR_OK) return st;
+  if (n == 0) return QR_OK;
+  if (!aligned16(in) || !aligned16(enc)) return QR_ERR_ALIGN;
+  if (overlap(in, n * 2, enc, qr_encoded_bytes(fmt, n))) return QR_ERR_OVERLAP;
+
+  PipeParams p;
+  std::memset(&p, 0, sizeof p);
+  p.in[0] = in;
+  p.W = 1;
+  p.n = n;
+  p.nb = (n + 31) / 32;
+  p.ntiles = (n + kTileElems - 1) / kTileElems;
+  encoded_regions(f, n, enc, &p.codes, &p.scales, &p.zps, &p.fp_values);
+  p.err = device_error_word();
+  if (!p.err) return QR_ERR_CUDA;
+  return to_status(dispatch_pipeline(f, d, MODE_ENCODE, p, static_cast<cudaStream_t>(stream)));
+}
+
+qr_status qr_dequantize(qr_dtype dt, qr_format fmt, const void* enc, size_t n, void* out, void* stream) {
+  const int f = static_cast<int>(fmt), d = static_cast<int>(dt);
+  if (n && (!enc || !out)) return QR_ERR_NULL;
+  if (!valid_dtype(d)) return QR_ERR_DTYPE;
+  if (!valid_format(f)) return QR_ERR_FORMAT;
+  qr_status st = check_size(n);
+  if (st != QR_OK) return st;
+  if (n == 0) return QR_OK;
+  if (!aligned16(enc) || !aligned16(out)) return QR_ERR_ALIGN;
+  if (overlap(enc, qr_encoded_bytes(fmt, n), out, n * 2)) return QR_ERR_OVERLAP;
+
+  DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  uint8_t* codes;
+  uint16_t *scales, *zps, *fpv;
+  encoded_regions(f, n, const_cast<void*>(enc), &codes, &scales, &zps, &fpv);
+  p.codes = codes;
+  p.scales = scales;
+  p.zps = zps;
+  p.fp_values = fpv;
+  p.out = out;
+  p.n = n;
+  p.nb = (n + 31) / 32;
+  p.err = device_error_word();
+  if (!p.err) return QR_ERR_CUDA;
+  return to_status(dispatch_decode(f, d, p, static_cast<cudaStream_t>(stream)));
+}
+
+qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages, const void* const* inputs,
+                                size_t n, void* out, void* wire, void* stream) {
+  const int f = static_cast<int>(fmt), d = static_cast<int>(dt);
+  if (n && (!inputs || !out)) return QR_ERR_NULL;
+  if (!valid_dtype(d)) return QR_ERR_DTYPE;
+  if (!valid_format(f)) return QR_ERR_FORMAT;
+  if (W != 1 && W != 2 && W != 4 && W != 8) return QR_ERR_WORLD;
+  if (stages != 1 && stages != 2) return QR_ERR_STAGES;
+  if (stages == 1 && wire) return QR_ERR_STAGES;
+  qr_status st = check_size(n);
+  if (st != QR_OK) return st;
+  if (n == 0) return QR_OK;
+  for (int r = 0; r < W; ++r)
+    if (!inputs[r]) return QR_ERR_NULL;
+  if (!aligned16(out) || (wire && !aligned16(wire))) return QR_ERR_ALIGN;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(inputs[r])) return QR_ERR_ALIGN;
+  const size_t msg = n * 2, wbytes = wire ? qr_encoded_bytes(fmt, n) : 0;
+  for (int r = 0; r < W; ++r)
+    if (overlap(inputs[r], msg, out, msg) || overlap(inputs[r], msg, wire, wbytes)) return QR_ERR_OVERLAP;
+  if (overlap(out, msg, wire, wbytes)) return QR_ERR_OVERLAP;
+
+  PipeParams p;
+  std::memset(&p, 0, sizeof p);
+  for (int r = 0; r < W; ++r) p.in[r] = inputs[r];
+  p.W = W;
+  p.n = n;
+  p.nb = (n + 31) / 32;
+  p.ntiles = (n + kTileElems - 1) / kTileElems;
+  p.out = out;
+  if (stages == 2) encoded_regions(f, n, wire, &p.codes, &p.scales, &p.zps, &p.fp_values);
+  p.err = device_error_word();
+  if (!p.err) return QR_ERR_CUDA;
+  const int mode = stages == 1 ? MODE_AR1 : MODE_AR2;
+  return to_status(dispatch_pipeline(f, d, mode, p, static_cast<cudaStream_t>(stream)));
+}
+
+qr_status qr_device_error(unsigned int* flags, int clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return QR_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_qr_error_flags, sizeof v) != cudaSuccess) return QR_ERR_CUDA;
+  if (clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_qr_error_flags, &zero, sizeof zero) != cudaSuccess) return QR_ERR_CUDA;
+  }
+  if (flags) *flags = v;
+  return v ? QR_ERR_DEVICE : QR_OK;
+}
+
+}  // extern "C"

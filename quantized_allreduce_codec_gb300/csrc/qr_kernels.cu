@@ -1,0 +1,85 @@
+// qr_kernels.cu -- kernel instantiations and launchers for ONE format,
+// selected at compile time with -DQR_FMT=<n> (the build compiles this file
+// once per format, in parallel).
+#include "qr_launch.h"
+
+#ifndef QR_FMT
+#error "compile with -DQR_FMT=<format number>"
+#endif
+
+#define QR_CAT2(a, b) a##b
+#define QR_CAT(a, b) QR_CAT2(a, b)
+
+namespace qr {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+template <int F, int D, int M>
+cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
+  // Per-device launch geometry, computed once (benign race: same values).
+  static int ctas_per_sm[kMaxDevices];
+  static int sm_count[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  auto kern = qr_pipeline_kernel<F, D, M>;
+  if (ctas_per_sm[dev] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int sms = 0, occ = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    sm_count[dev] = sms;
+    ctas_per_sm[dev] = occ > 0 ? occ : 1;
+  }
+  const unsigned long long max_grid = (unsigned long long)sm_count[dev] * ctas_per_sm[dev];
+  const unsigned grid = static_cast<unsigned>(p.ntiles < max_grid ? p.ntiles : max_grid);
+  kern<<<grid, kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int F, int D>
+cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
+  static int sm_count[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (sm_count[dev] == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev] = sms;
+  }
+  const unsigned long long want = (p.nb + 255) / 256;
+  const unsigned long long cap = (unsigned long long)sm_count[dev] * 8;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  qr_decode_kernel<F, D><<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t QR_CAT(launch_pipeline_fmt_, QR_FMT)(int dt, int mode, const PipeParams& p, cudaStream_t s) {
+  constexpr int F = QR_FMT;
+  if (dt == DT_F16) {
+    if (mode == MODE_ENCODE) return launch_pipe<F, DT_F16, MODE_ENCODE>(p, s);
+    if (mode == MODE_AR1) return launch_pipe<F, DT_F16, MODE_AR1>(p, s);
+    return launch_pipe<F, DT_F16, MODE_AR2>(p, s);
+  }
+  if (mode == MODE_ENCODE) return launch_pipe<F, DT_BF16, MODE_ENCODE>(p, s);
+  if (mode == MODE_AR1) return launch_pipe<F, DT_BF16, MODE_AR1>(p, s);
+  return launch_pipe<F, DT_BF16, MODE_AR2>(p, s);
+}
+
+cudaError_t QR_CAT(launch_decode_fmt_, QR_FMT)(int dt, const DecodeParams& p, cudaStream_t s) {
+  constexpr int F = QR_FMT;
+  if (dt == DT_F16) return launch_dec<F, DT_F16>(p, s);
+  return launch_dec<F, DT_BF16>(p, s);
+}
+
+}  // namespace qr

@@ -1,0 +1,134 @@
+"""The C ABI boundary, without a GPU: the library builds and loads, exports
+every function include/qr.h declares, agrees with the oracle's header and
+the quick_all_reduce page on enum values and encoded sizes, and rejects bad
+arguments on the host before any CUDA call."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import quantized_allreduce_codec_gb300 as qr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantized_allreduce_codec_gb300 import build
+    build.build()
+    return qr.lib()
+
+
+def header_functions(path):
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qr_[a-z_]+)\s*\(", text)))
+
+
+def header_enum(path, prefix):
+    text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+    return {k: int(v) for k, v in re.findall(rf"\b({prefix}[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+
+
+def test_exports_every_declared_function(L):
+    names = header_functions(os.path.join(ROOT, "include", "qr.h"))
+    assert set(names) == set(qr.EXPORTS)
+    for name in names:
+        assert hasattr(L, name), name
+    out = os.popen(f"nm -D --defined-only {qr.LIB_PATH}").read()
+    for name in names:
+        assert re.search(rf"\bT {name}\b", out), name
+
+
+def test_enums_agree_with_oracle_and_page():
+    lib_fmt = header_enum(os.path.join(ROOT, "include", "qr.h"), "QR_")
+    orc = header_enum(os.path.join(ROOT, "oracle", "qro.h"), "QRO_")
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "quick_reduce_regime.json")))
+    reg = g["QuickReduceRegime"]
+    assert lib_fmt["QR_FP"] == reg["FP"] == orc["QRO_FP"]
+    assert lib_fmt["QR_Q8"] == reg["INT8"] == orc["QRO_Q8"]
+    assert lib_fmt["QR_Q6"] == reg["INT6"] == orc["QRO_Q6"]
+    assert lib_fmt["QR_Q4"] == reg["INT4"] == orc["QRO_Q4"]
+    assert lib_fmt["QR_FP8"] == orc["QRO_FP8"]
+    assert lib_fmt["QR_Q8_ASYM"] == orc["QRO_Q8A"]
+    assert lib_fmt["QR_Q4_ASYM"] == orc["QRO_Q4A"]
+    assert lib_fmt["QR_F16"] == orc["QRO_F16"] and lib_fmt["QR_BF16"] == orc["QRO_BF16"]
+    for name, v in lib_fmt.items():
+        if name.startswith("QR_ERR") or name == "QR_OK":
+            assert qr.STATUS[v] == name
+
+
+@pytest.mark.parametrize("fmt", range(7))
+@pytest.mark.parametrize("n", [0, 8, 32, 40, 8192, 8200, 1 << 20])
+def test_encoded_bytes_match_oracle(L, oracle_mod, fmt, n):
+    assert qr.qr_encoded_bytes(fmt, n) == oracle_mod.encoded_bytes(fmt, n)
+
+
+def test_encoded_bytes_table():
+    # bytes per 32-element block: codes + fp16 scale (+ fp16 zero-point)
+    per_block = {qr.QR_Q8: 34, qr.QR_FP8: 34, qr.QR_Q6: 26, qr.QR_Q4: 18,
+                 qr.QR_Q8_ASYM: 36, qr.QR_Q4_ASYM: 20}
+    for f, b in per_block.items():
+        assert qr.qr_encoded_bytes(f, 32 * 1000) == 1000 * b
+    assert qr.qr_encoded_bytes(qr.QR_FP, 1000) == 2000
+    assert qr.qr_encoded_bytes(9, 1000) == 0
+
+
+def test_status_strings(L):
+    for s in range(len(qr.STATUS)):
+        assert qr.qr_status_string(s)
+    assert qr.qr_status_string(99) == "unknown status"
+
+
+# Host-side validation: fake, never dereferenced addresses.
+A, B, C = 0x10000, 0x200000, 0x4000000
+
+
+def _ar(W, dt, fmt, stages, inputs, n, out, wire=None):
+    arr = (ctypes.c_void_p * max(len(inputs), 1))(*inputs)
+    return qr.lib().qr_allreduce_emulated(W, dt, fmt, stages, ctypes.cast(arr, ctypes.c_void_p), n,
+                                          out, wire, None)
+
+
+def test_allreduce_argument_errors(L):
+    ok_in = [A, B]
+    assert _ar(2, 0, 1, 2, ok_in, 0, None) == 0                      # empty message: nothing to do
+    assert _ar(2, 0, 1, 2, ok_in, 64, None) == 1                     # QR_ERR_NULL
+    assert _ar(2, 0, 1, 2, [A, 0], 64, C) == 1                       # NULL rank pointer
+    assert _ar(2, 2, 1, 2, ok_in, 64, C) == 2                        # QR_ERR_DTYPE
+    assert _ar(2, 0, 7, 2, ok_in, 64, C) == 3                        # QR_ERR_FORMAT
+    assert _ar(3, 0, 1, 2, [A, B, A], 64, C) == 4                    # QR_ERR_WORLD
+    assert _ar(16, 0, 1, 2, ok_in * 8, 64, C) == 4
+    assert _ar(2, 0, 1, 3, ok_in, 64, C) == 5                        # QR_ERR_STAGES
+    assert _ar(2, 0, 1, 1, ok_in, 64, C, C + (1 << 20)) == 5         # wire with one stage
+    assert _ar(2, 0, 1, 2, ok_in, 60, C) == 6                        # 120 bytes: not % 16
+    assert _ar(2, 0, 1, 2, ok_in, (1 << 36) + 8, C) == 6             # too large
+    assert _ar(2, 0, 1, 2, [A + 2, B], 64, C) == 7                   # QR_ERR_ALIGN
+    assert _ar(2, 0, 1, 2, ok_in, 64, C + 8) == 7
+    assert _ar(2, 0, 1, 2, ok_in, 64, C, C + (1 << 20) + 4) == 7
+    assert _ar(2, 0, 1, 2, ok_in, 64, A + 64) == 8                   # out overlaps an input
+    assert _ar(2, 0, 1, 2, ok_in, 64, C, B + 16) == 8                # wire overlaps an input
+    assert _ar(2, 0, 1, 2, ok_in, 64, C, C + 64) == 8                # wire overlaps out
+
+
+def test_codec_argument_errors(L):
+    q, d = qr.lib().qr_quantize, qr.lib().qr_dequantize
+    assert q(0, 1, A, 0, None, None) == 0
+    assert q(0, 1, None, 64, B, None) == 1
+    assert q(5, 1, A, 64, B, None) == 2
+    assert q(0, 8, A, 64, B, None) == 3
+    assert q(0, 1, A, 12, B, None) == 6
+    assert q(0, 1, A + 8, 64, B, None) == 7
+    assert q(0, 1, A, 64, A + 16, None) == 8
+    assert d(0, 1, A, 64, None, None) == 1
+    assert d(1, 4, A, 64, A + 32, None) == 8
+    assert d(0, 2, A, 64, B + 2, None) == 7
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(qr, "_lib", None)
+    monkeypatch.setattr(qr, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        qr.lib()
