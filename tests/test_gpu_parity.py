@@ -223,12 +223,19 @@ def check_sampled(oracle_mod, wl_dtype, fmt, stages, xs_host, out, wire, n, seed
 
 
 def run_workload(oracle_mod, wl, fmts=None, stages_list=None, seed=0):
+    """Sampled blocks against the oracle, plus a property that holds at any
+    size: a second identical call gives the same bits everywhere (a pipeline
+    race shows up as run-to-run differences)."""
     xs = wl.inputs()
     dev = [dev_u16(x) for x in xs]
     for fmt in fmts or wl.formats:
         for stages in stages_list or wl.stages:
             out, wire = gpu_allreduce(wl.dtype, fmt, stages, None, dev_inputs=dev)
             check_sampled(oracle_mod, wl.dtype, fmt, stages, xs, out, wire, wl.n, seed + fmt)
+            out2, wire2 = gpu_allreduce(wl.dtype, fmt, stages, None, dev_inputs=dev)
+            assert_bits_equal(out2, out, "repeat")
+            if wire is not None:
+                assert np.array_equal(wire2, wire)
     del dev
     torch.cuda.empty_cache()
 
@@ -258,3 +265,19 @@ def test_workload4(oracle_mod):
 
 def test_workload5(oracle_mod):
     run_workload(oracle_mod, workloads()[5], seed=5)
+
+
+@pytest.mark.parametrize("fmt,stages", [(FP, 1), (Q8, 2), (Q4, 2)])
+def test_full_compare_64MiB(oracle_mod, fmt, stages):
+    """Every element of the tp2 table's largest message (W=2, fp16, 64 MiB
+    per rank), in the bench's launch configuration, against the oracle,
+    twice: a pipeline race would corrupt a few blocks anywhere."""
+    wl = sweep_workload(64 << 20)
+    xs = wl.inputs()
+    dev = [dev_u16(x) for x in xs]
+    o_out, o_wire = oracle_mod.allreduce(wl.dtype, fmt, stages, xs)
+    for _ in range(2):
+        out, wire = gpu_allreduce(wl.dtype, fmt, stages, None, dev_inputs=dev)
+        assert_bits_equal(out, o_out)
+        if stages == 2:
+            assert_encoded_equal(wire, o_wire, fmt, wl.n)
