@@ -6,9 +6,10 @@ One step = one pass of the whole hot path over the tp2 workload of the vLLM
 PR #18473 timing table at its largest size: W=2 emulated ranks, fp16,
 64 MiB per rank, N(0,1), in the table's six kernels -- FP one-stage, FP
 two-stage, FP8, Q8, Q6 and Q4 two-stage (every two-stage call also writes
-its stage-2 payload).  Inputs are resident in HBM; L2 is flushed (a write
-of at least twice its size) before every timed call, outside the timed
-events.
+its stage-2 payload).  Inputs are resident in HBM; L2 is flushed before every timed call,
+outside the timed events: a write of at least twice its size, then a read
+of a second buffer of that size, so that the flush leaves no dirty lines to
+be written back during the timed call.
 
 metric: GB/s per rank-message = sum of per-rank message bytes (n*2) over
 the calls / sum of their device times (CUDA events on the launching
@@ -228,9 +229,14 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+    clean_buf = torch.ones_like(flush_buf)
 
     def flush():
+        # write more than twice the L2 (evicts the inputs), then read a second
+        # buffer of that size so the dirty lines of the write are written back
+        # here rather than inside the next timed call
         flush_buf.fill_(1)
+        clean_buf.sum()
 
     wl = sweep_workload(BENCH_BYTES)
     n, W = wl.n, wl.W
@@ -407,7 +413,9 @@ def run_ours(args):
                                    "(33554432 elements) per rank, N(0,1) seed 2000+r; one step = "
                                    "FP 1-stage, FP 2-stage, FP8, Q8, Q6, Q4 2-stage (payload written)",
                        "W": W, "per_rank_bytes": n * 2, "calls_per_step": len(STEP_CALLS),
-                       "l2": f"flushed before every timed call ({flush_buf.numel() * 4 >> 20} MiB write)",
+                       "l2": f"flushed before every timed call, outside the timed events: a "
+                             f"{flush_buf.numel() * 4 >> 20} MiB write, then a {clean_buf.numel() * 4 >> 20} MiB "
+                             "read of a second buffer (no dirty lines left in L2)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, W ranks emulated in HBM"},
             "roofline": roofline, "per_format": per_format,
             "cpu_baseline": cpu, "e2e": e2e,
@@ -484,7 +492,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
