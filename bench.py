@@ -229,7 +229,7 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
-    clean_buf = torch.ones_like(flush_buf)
+    clean_buf = torch.ones(flush_buf.numel(), dtype=torch.float32, device=dev)
 
     def flush():
         # write more than twice the L2 (evicts the inputs), then read a second
@@ -361,6 +361,32 @@ def run_ours(args):
                                            "hbm_frac": round(bytes_alg(W, nn, fmt, st, st == 2) / t / 1e9 / peak, 3)}
             sweep[str(size)] = row
 
+    # ---------------- the codec on its own (qr_quantize / qr_dequantize) ----------------
+    codec = {}
+    if not args.no_extras:
+        src = ins[0]
+        for fmt in (FP8, Q8, Q6, Q4, Q8A, Q4A):
+            enc = torch.empty(encoded_bytes(fmt, n), dtype=torch.uint8, device=dev)
+            row = {}
+            for name, fn in (("quantize", lambda: qr.qr_quantize(wl.dtype, fmt, src, n, enc, stream)),
+                             ("dequantize", lambda: qr.qr_dequantize(wl.dtype, fmt, enc, n, out, stream))):
+                ts = []
+                for it in range(args.warmup + args.sweep_iters):
+                    flush()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    if it >= args.warmup:
+                        ts.append((a, b))
+                torch.cuda.synchronize()
+                t = float(np.median([x.elapsed_time(y) for x, y in ts])) * 1e-3
+                ba = n * 2 + encoded_bytes(fmt, n)
+                row[name] = {"us": round(t * 1e6, 2), "hbm_GBps": round(ba / t / 1e9, 1),
+                             "hbm_frac": round(ba / t / 1e9 / peak, 3)}
+            codec[FORMAT_NAMES[fmt]] = row
+            del enc
+
     # ---------------- the other workloads ----------------
     extra = {}
     if not args.no_extras:
@@ -421,7 +447,7 @@ def run_ours(args):
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": K * len(STEP_CALLS),
             "clocks": clocks, "wall_ms_per_step_incl_flush": round(wall / K * 1e3, 3),
-            "sweep_W2_fp16": sweep, "workloads": extra,
+            "sweep_W2_fp16": sweep, "codec_fp16_64MiB": codec, "workloads": extra,
         }
         print(json.dumps(line), flush=True)
     dist_barrier()
