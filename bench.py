@@ -12,8 +12,11 @@ of a second buffer of that size, so that the flush leaves no dirty lines to
 be written back during the timed call.
 
 metric: GB/s per rank-message = sum of per-rank message bytes (n*2) over
-the calls / sum of their device times (CUDA events on the launching
-stream).  The JSON line also carries the HBM roofline of the fused
+the calls / their device time.  The timed region is K replays of a CUDA
+graph holding one step (each call preceded by its L2 flush), timed with
+CUDA events; the same graph without the qr calls is replayed K times and
+its time subtracted.  Eager per-call event times are reported beside it
+(they include a ~4 us launch gap that even an empty kernel shows).  The JSON line also carries the HBM roofline of the fused
 two-stage quantized kernel, the oracle's CPU rate on a bounded sample, an
 end-to-end rate through the C ABI with host buffers, a size sweep, and the
 other workloads.
@@ -224,7 +227,6 @@ def run_ours(args):
     dist_barrier()
     qr.lib()
     dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
 
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
@@ -245,11 +247,13 @@ def run_ours(args):
     out = torch.empty(n, dtype=torch.int16, device=dev)
     wires = {f: torch.empty(encoded_bytes(f, n), dtype=torch.uint8, device=dev) for f, _ in STEP_CALLS}
 
-    def call(fmt, stages, inputs=ins, nn=n, o=out):
+    def call(fmt, stages, inputs=None, nn=n, o=out):
+        # stream=None: torch's current stream (the capture stream inside a graph)
+        inputs = ins if inputs is None else inputs
         qr.qr_allreduce_emulated(len(inputs), wl.dtype, fmt, stages, inputs, nn, o,
-                                 wires[fmt] if stages == 2 else None, stream)
+                                 wires[fmt] if stages == 2 else None, None)
 
-    # warm-up (also first-call set-up of every instantiation used)
+    # warm-up, eager (also first-call set-up of every instantiation used)
     for _ in range(args.warmup):
         for fmt, st in STEP_CALLS:
             flush()
@@ -258,48 +262,101 @@ def run_ours(args):
     if qr.qr_device_error() != 0:
         raise RuntimeError("kernel wait-limit flag raised during warm-up")
 
+    # The timed work runs as CUDA-graph replays: one step = the six calls, each
+    # preceded by an L2 flush.  A second graph holds the same six flushes and
+    # nothing else; its time is subtracted, so the reported time is the qr
+    # kernels' device time with launch latency overlapped as in any stream of
+    # work (eager per-call events, reported beside it, also count the ~4 us
+    # launch gap an empty kernel shows between two events).
+    cap_stream = torch.cuda.Stream(device=dev)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap_stream):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    def replay_time(g, reps):
+        s = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(reps):
+            g.replay()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e-3
+
+    flush_graphs = {}
+
+    def per_call_seconds(fn, reps):
+        """Device time of fn per call: [flush, fn] x reps minus [flush] x reps."""
+        fn()  # eager first call: any one-time set-up happens outside capture
+        torch.cuda.synchronize()
+        g1 = capture(lambda: [(flush(), fn()) for _ in range(reps)])
+        if reps not in flush_graphs:
+            flush_graphs[reps] = capture(lambda: [flush() for _ in range(reps)])
+        g0 = flush_graphs[reps]
+        for g in (g1, g0):
+            g.replay()
+        t1 = replay_time(g1, 2) / 2
+        t0 = replay_time(g0, 2) / 2
+        del g1
+        return max((t1 - t0) / reps, 1e-9)
+
+    step_graph = capture(lambda: [(flush(), call(fmt, st)) for fmt, st in STEP_CALLS])
+    flush_graph = capture(lambda: [flush() for _ in STEP_CALLS])
+    for _ in range(args.warmup):
+        step_graph.replay()
+        flush_graph.replay()
+    torch.cuda.synchronize()
+
     K = args.steps
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in STEP_CALLS] for _ in range(K)]
     sampler = ClockSampler(smi_device_id(props, local))
     dist_barrier()
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.2)
     wall0 = time.perf_counter()
-    for k in range(K):
-        for j, (fmt, st) in enumerate(STEP_CALLS):
-            flush()
-            ev[k][j][0].record(stream)
-            call(fmt, st)
-            ev[k][j][1].record(stream)
-    torch.cuda.synchronize()
+    t_steps = replay_time(step_graph, K)          # K timed steps (synchronised on both sides)
     wall = time.perf_counter() - wall0
     dist_barrier()
     clocks = sampler.stop()
+    t_flush = replay_time(flush_graph, K)         # the same flushes alone
     if qr.qr_device_error() != 0:
         raise RuntimeError("kernel wait-limit flag raised in the timed region")
-
-    times = np.array([[a.elapsed_time(b) * 1e-3 for a, b in row] for row in ev])  # seconds [K, calls]
-    per_call = times.sum(axis=0) / K
-    my_total = float(times.sum())
+    my_total = t_steps - t_flush
     max_total = dist_max(my_total, dev)
     step_bytes = sum(n * 2 for _ in STEP_CALLS)
     value = aggregate(K * step_bytes, max_total, world)
 
+    # per-call device times (graphs) and eager event times, for the breakdown
     peak, peak_kind = read_peaks()
     per_format = {}
     q_bytes = q_time = 0.0
-    for j, (fmt, st) in enumerate(STEP_CALLS):
+    stream = torch.cuda.current_stream()
+    for fmt, st in STEP_CALLS:
         b = bytes_alg(W, n, fmt, st, st == 2)
-        t = float(np.median(times[:, j]))
+        t = per_call_seconds(lambda: call(fmt, st), args.graph_reps)
+        eager = []
+        for it in range(args.warmup + args.sweep_iters):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(fmt, st)
+            e1.record(stream)
+            if it >= args.warmup:
+                eager.append((e0, e1))
+        torch.cuda.synchronize()
+        te = float(np.median([x.elapsed_time(y) for x, y in eager])) * 1e-3
         per_format[step_name(fmt, st)] = {
-            "us_median": round(t * 1e6, 2), "us_min": round(float(times[:, j].min()) * 1e6, 2),
+            "us": round(t * 1e6, 2), "us_eager_events": round(te * 1e6, 2),
             "algbw_GBps": round(n * 2 / t / 1e9, 1), "hbm_GBps": round(b / t / 1e9, 1),
             "frac_of_measured_peak": round(b / t / 1e9 / peak, 3)}
         if fmt != FP:
-            q_bytes += b * K
-            q_time += float(times[:, j].sum())
+            q_bytes += b
+            q_time += t
     achieved = q_bytes / q_time / 1e9
     traffic = recorded_traffic(os.path.join(ROOT, "quantized_allreduce_codec_gb300", "csrc",
                                             "qr_device.cuh"))
@@ -310,9 +367,11 @@ def run_ours(args):
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "frac_of_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": (float(traffic["bytes_per_launch"]) if traffic else None),
-                "algorithmic_bytes_per_launch": round(q_bytes / (4 * K)),
+                "algorithmic_bytes_per_launch": round(q_bytes / 4),
                 "traffic_note": (traffic.get("note") if traffic else
-                                 "no ncu capture of the current kernel source")}
+                                 "no ncu capture of the current kernel source"),
+                "timing": f"per-call device time from CUDA-graph replays ({args.graph_reps} calls, "
+                          "flush-only graph subtracted)"}
 
     # ---------------- end to end through the C ABI, host buffers ----------------
     Ke = max(1, min(args.steps, args.e2e_steps))
@@ -341,24 +400,25 @@ def run_ours(args):
     # ---------------- size sweep (tp2 table sizes) ----------------
     sweep = {}
     if not args.no_extras:
+        default_limit = qr.qr_direct_limit()
         for size in sweep_sizes_bytes():
             nn = size // 2
             sub = [t[:nn] for t in ins]
             row = {}
+            # both kernels are timed at every size (the default routing picks one)
+            paths = [("default", default_limit), ("direct", (1 << 64) - 1), ("pipeline", 0)]
             for fmt, st in STEP_CALLS:
-                ts = []
-                for it in range(args.warmup + args.sweep_iters):
-                    flush()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    call(fmt, st, sub, nn, out)
-                    b.record(stream)
-                    if it >= args.warmup:
-                        ts.append((a, b))
-                torch.cuda.synchronize()
-                t = float(np.median([x.elapsed_time(y) for x, y in ts])) * 1e-3
-                row[step_name(fmt, st)] = {"us": round(t * 1e6, 2),
-                                           "hbm_frac": round(bytes_alg(W, nn, fmt, st, st == 2) / t / 1e9 / peak, 3)}
+                entry = {}
+                for pname, limit in paths:
+                    qr.qr_set_direct_limit(limit)
+                    t = per_call_seconds(lambda: call(fmt, st, sub, nn, out), args.sweep_reps)
+                    if pname == "default":
+                        entry.update({"us": round(t * 1e6, 2),
+                                      "hbm_frac": round(bytes_alg(W, nn, fmt, st, st == 2) / t / 1e9 / peak, 3)})
+                    else:
+                        entry[f"us_{pname}"] = round(t * 1e6, 2)
+                qr.qr_set_direct_limit(default_limit)
+                row[step_name(fmt, st)] = entry
             sweep[str(size)] = row
 
     # ---------------- the codec on its own (qr_quantize / qr_dequantize) ----------------
@@ -367,20 +427,11 @@ def run_ours(args):
         src = ins[0]
         for fmt in (FP8, Q8, Q6, Q4, Q8A, Q4A):
             enc = torch.empty(encoded_bytes(fmt, n), dtype=torch.uint8, device=dev)
+            qr.qr_quantize(wl.dtype, fmt, src, n, enc)
             row = {}
-            for name, fn in (("quantize", lambda: qr.qr_quantize(wl.dtype, fmt, src, n, enc, stream)),
-                             ("dequantize", lambda: qr.qr_dequantize(wl.dtype, fmt, enc, n, out, stream))):
-                ts = []
-                for it in range(args.warmup + args.sweep_iters):
-                    flush()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    fn()
-                    b.record(stream)
-                    if it >= args.warmup:
-                        ts.append((a, b))
-                torch.cuda.synchronize()
-                t = float(np.median([x.elapsed_time(y) for x, y in ts])) * 1e-3
+            for name, fn in (("quantize", lambda: qr.qr_quantize(wl.dtype, fmt, src, n, enc)),
+                             ("dequantize", lambda: qr.qr_dequantize(wl.dtype, fmt, enc, n, out))):
+                t = per_call_seconds(fn, args.sweep_reps)
                 ba = n * 2 + encoded_bytes(fmt, n)
                 row[name] = {"us": round(t * 1e6, 2), "hbm_GBps": round(ba / t / 1e9, 1),
                              "hbm_frac": round(ba / t / 1e9 / peak, 3)}
@@ -400,18 +451,10 @@ def run_ours(args):
             for fmt in w.formats:
                 wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
                 for st in w.stages:
-                    ts = []
-                    for it in range(args.warmup + args.sweep_iters):
-                        flush()
-                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                        a.record(stream)
-                        qr.qr_allreduce_emulated(w.W, w.dtype, fmt, st, dins, w.n, o,
-                                                 wire if st == 2 else None, stream)
-                        b.record(stream)
-                        if it >= args.warmup:
-                            ts.append((a, b))
-                    torch.cuda.synchronize()
-                    t = float(np.median([x.elapsed_time(y) for x, y in ts])) * 1e-3
+                    t = per_call_seconds(
+                        lambda: qr.qr_allreduce_emulated(w.W, w.dtype, fmt, st, dins, w.n, o,
+                                                         wire if st == 2 else None, None),
+                        args.sweep_reps)
                     ba = bytes_alg(w.W, w.n, fmt, st, st == 2)
                     res[step_name(fmt, st)] = {"us": round(t * 1e6, 1),
                                                "algbw_GBps": round(w.n * 2 / t / 1e9, 1),
@@ -433,6 +476,8 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(max_total / K * 1e3, 4),
+            "timing": "K replays of a CUDA graph holding one step (six [L2 flush, qr call] pairs), "
+                      "timed with CUDA events, minus K replays of the same graph without the qr calls",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": "tp2 table, largest size: W=2 emulated ranks, fp16, 64 MiB "
@@ -447,6 +492,7 @@ def run_ours(args):
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": K * len(STEP_CALLS),
             "clocks": clocks, "wall_ms_per_step_incl_flush": round(wall / K * 1e3, 3),
+            "flush_ms_per_step": round(t_flush / K * 1e3, 4),
             "sweep_W2_fp16": sweep, "codec_fp16_64MiB": codec, "workloads": extra,
         }
         print(json.dumps(line), flush=True)
@@ -523,6 +569,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--graph-reps", type=int, default=50, help="calls per graph for per-call times")
+    ap.add_argument("--sweep-reps", type=int, default=10, help="calls per graph in the sweep/extras")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-elems", type=int, default=1 << 18)
     ap.add_argument("--no-extras", action="store_true", help="skip the size sweep and other workloads")

@@ -140,6 +140,16 @@ qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages,
                                 const void *const *inputs, size_t n,
                                 void *out, void *wire, void *stream);
 
+/* Messages of at most qr_direct_limit() elements per rank are processed by a
+ * single-pass kernel with one memory round trip (lowest latency); longer ones
+ * by the persistent bulk-copy pipeline (highest bandwidth).  Both compute
+ * identical bits.  The default limit is 4194304 elements (8 MiB of fp16);
+ * qr_set_direct_limit changes it for the whole process (0: always the
+ * pipeline; SIZE_MAX: always the direct kernel).  Host only, no CUDA call;
+ * applies to qr_quantize and qr_allreduce_emulated calls made afterwards. */
+size_t qr_direct_limit(void);
+void qr_set_direct_limit(size_t n);
+
 /* A short English description of a status code (static storage). */
 const char *qr_status_string(qr_status st);
 

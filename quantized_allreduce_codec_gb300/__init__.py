@@ -25,7 +25,7 @@ STATUS = ["QR_OK", "QR_ERR_NULL", "QR_ERR_DTYPE", "QR_ERR_FORMAT", "QR_ERR_WORLD
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqr.so")
 EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
-           "qr_status_string", "qr_device_error")
+           "qr_status_string", "qr_device_error", "qr_direct_limit", "qr_set_direct_limit")
 
 _lib = None
 _lock = threading.Lock()
@@ -63,6 +63,10 @@ def lib():
                 L.qr_status_string.argtypes = [i]
                 L.qr_device_error.restype = i
                 L.qr_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
+                L.qr_direct_limit.restype = sz
+                L.qr_direct_limit.argtypes = []
+                L.qr_set_direct_limit.restype = None
+                L.qr_set_direct_limit.argtypes = [sz]
                 _lib = L
     return _lib
 
@@ -139,3 +143,13 @@ def qr_device_error(clear: bool = True) -> int:
     if st not in (0, 10):
         raise QRError(st, "qr_device_error")
     return int(flags.value)
+
+
+def qr_direct_limit() -> int:
+    """Largest message (elements per rank) handled by the direct kernel."""
+    return int(lib().qr_direct_limit())
+
+
+def qr_set_direct_limit(n: int) -> None:
+    """Set the direct-kernel limit for the process (0: always the pipeline)."""
+    lib().qr_set_direct_limit(n)

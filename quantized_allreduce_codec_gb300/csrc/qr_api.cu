@@ -2,6 +2,7 @@
 // validation, encoded-buffer layout, dispatch to the per-format launchers.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -15,6 +16,7 @@ __device__ unsigned g_qr_error_flags;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultDirectLimit = 4ull * 1024 * 1024;  // elements per rank (8 MiB of fp16)
 
 int code_bits(int fmt) {
   switch (fmt) {
@@ -41,7 +43,24 @@ qr_status check_size(size_t n) {
 
 qr_status to_status(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_CUDA; }
 
+// Messages of at most this many elements per rank take the direct kernel.
+std::atomic<unsigned long long> g_direct_limit{kDefaultDirectLimit};
+
+cudaError_t dispatch_direct(int fmt, int dt, int mode, const PipeParams& p, cudaStream_t s) {
+  switch (fmt) {
+    case 0: return launch_direct_fmt_0(dt, mode, p, s);
+    case 1: return launch_direct_fmt_1(dt, mode, p, s);
+    case 2: return launch_direct_fmt_2(dt, mode, p, s);
+    case 3: return launch_direct_fmt_3(dt, mode, p, s);
+    case 4: return launch_direct_fmt_4(dt, mode, p, s);
+    case 5: return launch_direct_fmt_5(dt, mode, p, s);
+    case 6: return launch_direct_fmt_6(dt, mode, p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t dispatch_pipeline(int fmt, int dt, int mode, const PipeParams& p, cudaStream_t s) {
+  if (p.n <= g_direct_limit.load(std::memory_order_relaxed)) return dispatch_direct(fmt, dt, mode, p, s);
   switch (fmt) {
     case 0: return launch_pipeline_fmt_0(dt, mode, p, s);
     case 1: return launch_pipeline_fmt_1(dt, mode, p, s);
@@ -218,6 +237,10 @@ qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages, c
   const int mode = stages == 1 ? MODE_AR1 : MODE_AR2;
   return to_status(dispatch_pipeline(f, d, mode, p, static_cast<cudaStream_t>(stream)));
 }
+
+size_t qr_direct_limit(void) { return static_cast<size_t>(g_direct_limit.load()); }
+
+void qr_set_direct_limit(size_t n) { g_direct_limit.store(static_cast<unsigned long long>(n)); }
 
 qr_status qr_device_error(unsigned int* flags, int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return QR_ERR_CUDA;

@@ -42,6 +42,26 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int F, int D, int M>
+cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
+  static int sm_count[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (sm_count[dev] == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev] = sms;
+  }
+  const unsigned long long want = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;
+  const unsigned long long cap = (unsigned long long)sm_count[dev] * 16;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  qr_direct_kernel<F, D, M><<<grid, kDirectThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 template <int F, int D>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
   static int sm_count[kMaxDevices];
@@ -55,10 +75,11 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     sm_count[dev] = sms;
   }
-  const unsigned long long want = (p.nb + 255) / 256;
+  const unsigned long long per_cta = (unsigned long long)kDecodeThreads * kDecodeUnroll;
+  const unsigned long long want = (p.n / 8 + per_cta - 1) / per_cta;
   const unsigned long long cap = (unsigned long long)sm_count[dev] * 8;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  qr_decode_kernel<F, D><<<grid, 256, 0, s>>>(p);
+  qr_decode_kernel<F, D><<<grid, kDecodeThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -74,6 +95,18 @@ cudaError_t QR_CAT(launch_pipeline_fmt_, QR_FMT)(int dt, int mode, const PipePar
   if (mode == MODE_ENCODE) return launch_pipe<F, DT_BF16, MODE_ENCODE>(p, s);
   if (mode == MODE_AR1) return launch_pipe<F, DT_BF16, MODE_AR1>(p, s);
   return launch_pipe<F, DT_BF16, MODE_AR2>(p, s);
+}
+
+cudaError_t QR_CAT(launch_direct_fmt_, QR_FMT)(int dt, int mode, const PipeParams& p, cudaStream_t s) {
+  constexpr int F = QR_FMT;
+  if (dt == DT_F16) {
+    if (mode == MODE_ENCODE) return launch_dir<F, DT_F16, MODE_ENCODE>(p, s);
+    if (mode == MODE_AR1) return launch_dir<F, DT_F16, MODE_AR1>(p, s);
+    return launch_dir<F, DT_F16, MODE_AR2>(p, s);
+  }
+  if (mode == MODE_ENCODE) return launch_dir<F, DT_BF16, MODE_ENCODE>(p, s);
+  if (mode == MODE_AR1) return launch_dir<F, DT_BF16, MODE_AR1>(p, s);
+  return launch_dir<F, DT_BF16, MODE_AR2>(p, s);
 }
 
 cudaError_t QR_CAT(launch_decode_fmt_, QR_FMT)(int dt, const DecodeParams& p, cudaStream_t s) {

@@ -76,6 +76,16 @@ def test_encoded_bytes_table():
     assert qr.qr_encoded_bytes(9, 1000) == 0
 
 
+def test_direct_limit_knob(L):
+    old = qr.qr_direct_limit()
+    try:
+        qr.qr_set_direct_limit(12345)
+        assert qr.qr_direct_limit() == 12345
+    finally:
+        qr.qr_set_direct_limit(old)
+    assert qr.qr_direct_limit() == old
+
+
 def test_status_strings(L):
     for s in range(len(qr.STATUS)):
         assert qr.qr_status_string(s)

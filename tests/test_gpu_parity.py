@@ -33,6 +33,16 @@ def library():
     assert qr.qr_device_error(clear=True) == 0, "a kernel raised its wait-limit flag"
 
 
+@pytest.fixture(params=["direct", "pipeline"])
+def path(request):
+    """Run the test once through each kernel: the direct (small-message)
+    kernel and the bulk-copy pipeline kernel."""
+    old = qr.qr_direct_limit()
+    qr.qr_set_direct_limit((1 << 64) - 1 if request.param == "direct" else 0)
+    yield request.param
+    qr.qr_set_direct_limit(old)
+
+
 def spread_values(rng, n, dtype, zero_blocks=True):
     """N(0,1) with per-block magnitudes from 2^-20 to 2^12 (bf16: to 2^40),
     a few all-zero and constant blocks, and some negative zeros."""
@@ -76,7 +86,7 @@ def assert_bits_equal(got, want, what="out"):
 @pytest.mark.parametrize("n", SMALL_SIZES)
 @pytest.mark.parametrize("fmt", ALL_FORMATS)
 @pytest.mark.parametrize("dtype", [F16, BF16])
-def test_quantize_parity(oracle_mod, dtype, fmt, n):
+def test_quantize_parity(oracle_mod, dtype, fmt, n, path):
     xb = spread_values(np.random.default_rng(1000 + n + 17 * fmt), n, dtype)
     assert_encoded_equal(gpu_quantize(dtype, fmt, xb), oracle_mod.quantize(dtype, fmt, xb), fmt, n)
 
@@ -115,7 +125,7 @@ def test_dequantize_arbitrary_codes(oracle_mod, dtype, fmt):
 @pytest.mark.parametrize("fmt", ALL_FORMATS)
 @pytest.mark.parametrize("dtype", [F16, BF16])
 @pytest.mark.parametrize("W", [1, 2, 4, 8])
-def test_allreduce_parity(oracle_mod, W, dtype, fmt, stages, n):
+def test_allreduce_parity(oracle_mod, W, dtype, fmt, stages, n, path):
     rng = np.random.default_rng(4000 + 7 * W + 13 * fmt + n + stages)
     xs = [spread_values(rng, n, dtype, zero_blocks=(r == 0)) for r in range(W)]
     out, wire = gpu_allreduce(dtype, fmt, stages, xs)
@@ -126,7 +136,7 @@ def test_allreduce_parity(oracle_mod, W, dtype, fmt, stages, n):
 
 
 @pytest.mark.parametrize("fmt", ALL_FORMATS)
-def test_allreduce_without_wire_gives_same_output(oracle_mod, fmt):
+def test_allreduce_without_wire_gives_same_output(oracle_mod, fmt, path):
     rng = np.random.default_rng(5000 + fmt)
     n = 2 * 8192 + 24
     xs = [to_bits(rng.standard_normal(n).astype(np.float32), F16) for _ in range(4)]
@@ -136,7 +146,7 @@ def test_allreduce_without_wire_gives_same_output(oracle_mod, fmt):
 
 
 @pytest.mark.parametrize("fmt", [FP, Q8, Q6, Q4A])
-def test_result_independent_of_tile_assignment(fmt):
+def test_result_independent_of_tile_assignment(fmt, path):
     """Starting the same data 3 tiles + 5 blocks later (so every block lands
     on a different thread, rotation and CTA) gives the same blocks."""
     rng = np.random.default_rng(6000 + fmt)
@@ -155,7 +165,7 @@ def test_result_independent_of_tile_assignment(fmt):
 
 
 @pytest.mark.parametrize("dtype", [F16, BF16])
-def test_degenerate_blocks(oracle_mod, dtype):
+def test_degenerate_blocks(oracle_mod, dtype, path):
     """All-zero, constant, negative-zero, underflowing and (bf16) saturating
     blocks through every format and both stage counts."""
     n = 32 * 64
@@ -281,3 +291,23 @@ def test_full_compare_64MiB(oracle_mod, fmt, stages):
         assert_bits_equal(out, o_out)
         if stages == 2:
             assert_encoded_equal(wire, o_wire, fmt, wl.n)
+
+
+def test_direct_limit_default_and_paths_agree(oracle_mod):
+    """The default limit routes small messages to the direct kernel; both
+    kernels give the same bits on a message that straddles the limit."""
+    assert qr.qr_direct_limit() == 4 * 1024 * 1024
+    rng = np.random.default_rng(7000)
+    n = 4 * 1024 * 1024 + 8
+    xs = [to_bits(rng.standard_normal(n).astype(np.float32), F16) for _ in range(2)]
+    old = qr.qr_direct_limit()
+    try:
+        for fmt in (Q8, Q6, Q4A):
+            qr.qr_set_direct_limit(0)
+            a, wa = gpu_allreduce(F16, fmt, 2, xs)
+            qr.qr_set_direct_limit((1 << 64) - 1)
+            b, wb = gpu_allreduce(F16, fmt, 2, xs)
+            assert_bits_equal(a, b, "paths")
+            assert np.array_equal(wa, wb)
+    finally:
+        qr.qr_set_direct_limit(old)
