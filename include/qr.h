@@ -153,10 +153,20 @@ void qr_set_direct_limit(size_t n);
 /* A short English description of a status code (static storage). */
 const char *qr_status_string(qr_status st);
 
+/* Self-test of the kernels' bounded waits, for tests of the failure path:
+ * launches one warp that waits on a shared-memory barrier nothing will
+ * complete, through the same bounded-wait routine the pipeline kernel uses,
+ * with a limit of limit_us microseconds (1 .. 1000000; otherwise
+ * QR_ERR_SIZE).  When the limit expires the wait gives up, the kernel sets
+ * flag 8 in the device flag word and returns; read it with
+ * qr_device_error().  Nothing faults and nothing hangs. */
+qr_status qr_selftest_wait_timeout(unsigned int limit_us, void *stream);
+
 /* Kernels never wait forever: a pipeline wait that exceeds its time limit
  * sets a flag in device memory and the kernel returns early.  This call
  * synchronises the current device, copies the flags to *flags (0 = none
- * raised) and clears them when clear != 0.  Returns QR_ERR_DEVICE when a
+ * raised; 1 = a consumer wait, 2 = a producer wait, 4 = the final drain,
+ * 8 = the self-test) and clears them when clear != 0.  Returns QR_ERR_DEVICE when a
  * flag was raised, QR_OK otherwise, QR_ERR_CUDA on a CUDA error. */
 qr_status qr_device_error(unsigned int *flags, int clear);
 

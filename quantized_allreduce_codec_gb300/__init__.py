@@ -25,7 +25,8 @@ STATUS = ["QR_OK", "QR_ERR_NULL", "QR_ERR_DTYPE", "QR_ERR_FORMAT", "QR_ERR_WORLD
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqr.so")
 EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
-           "qr_status_string", "qr_device_error", "qr_direct_limit", "qr_set_direct_limit")
+           "qr_status_string", "qr_device_error", "qr_direct_limit", "qr_set_direct_limit",
+           "qr_selftest_wait_timeout")
 
 _lib = None
 _lock = threading.Lock()
@@ -67,6 +68,8 @@ def lib():
                 L.qr_direct_limit.argtypes = []
                 L.qr_set_direct_limit.restype = None
                 L.qr_set_direct_limit.argtypes = [sz]
+                L.qr_selftest_wait_timeout.restype = i
+                L.qr_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
                 _lib = L
     return _lib
 
@@ -153,3 +156,8 @@ def qr_direct_limit() -> int:
 def qr_set_direct_limit(n: int) -> None:
     """Set the direct-kernel limit for the process (0: always the pipeline)."""
     lib().qr_set_direct_limit(n)
+
+
+def qr_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (raises device flag 8 after limit_us)."""
+    _check(lib().qr_selftest_wait_timeout(limit_us, _stream(stream)), "qr_selftest_wait_timeout")

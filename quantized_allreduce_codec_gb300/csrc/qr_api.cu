@@ -104,6 +104,19 @@ void encoded_regions(int fmt, size_t n, void* base, uint8_t** codes, uint16_t** 
   if (is_asym(fmt)) *zps = reinterpret_cast<uint16_t*>(b + nb * cb + 2 * nb);
 }
 
+// One warp waits on a shared-memory barrier that nothing will complete; the
+// bounded wait gives up after limit_ns and raises kErrSelfTest.
+__global__ void qr_selftest_wait_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool completed = mbar_wait(&bar, 0u, limit_ns);
+  if (!__all_sync(0xffffffffu, completed) && threadIdx.x == 0) atomicOr(err, kErrSelfTest);
+}
+
 }  // namespace
 
 unsigned* device_error_word() {
@@ -241,6 +254,15 @@ qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages, c
 size_t qr_direct_limit(void) { return static_cast<size_t>(g_direct_limit.load()); }
 
 void qr_set_direct_limit(size_t n) { g_direct_limit.store(static_cast<unsigned long long>(n)); }
+
+qr_status qr_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 1000000u) return QR_ERR_SIZE;
+  unsigned* err = device_error_word();
+  if (!err) return QR_ERR_CUDA;
+  qr_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      err, static_cast<unsigned long long>(limit_us) * 1000ull);
+  return to_status(cudaGetLastError());
+}
 
 qr_status qr_device_error(unsigned int* flags, int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return QR_ERR_CUDA;

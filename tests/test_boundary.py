@@ -135,6 +135,8 @@ def test_codec_argument_errors(L):
     assert d(0, 1, A, 64, None, None) == 1
     assert d(1, 4, A, 64, A + 32, None) == 8
     assert d(0, 2, A, 64, B + 2, None) == 7
+    assert qr.lib().qr_selftest_wait_timeout(0, None) == 6           # limit out of range
+    assert qr.lib().qr_selftest_wait_timeout(1000001, None) == 6
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
