@@ -51,31 +51,34 @@ def build(force: bool = False) -> str:
         return _LIB
 
 
+def _bind(lib):
+    u16, u8, f32 = ctypes.c_uint16, ctypes.c_uint8, ctypes.c_float
+    sz, i = ctypes.c_size_t, ctypes.c_int
+    vp = ctypes.c_void_p
+    for name, res, args in [
+        ("qro_f16_to_f32", f32, [u16]),
+        ("qro_f32_to_f16", u16, [f32]),
+        ("qro_f32_to_f16_satfinite", u16, [f32]),
+        ("qro_bf16_to_f32", f32, [u16]),
+        ("qro_f32_to_bf16", u16, [f32]),
+        ("qro_e4m3_to_f32", f32, [u8]),
+        ("qro_f32_to_e4m3_satfinite", u8, [f32]),
+        ("qro_encoded_bytes", sz, [i, sz]),
+        ("qro_quantize", i, [i, i, vp, sz, vp]),
+        ("qro_dequantize", i, [i, i, vp, sz, vp]),
+        ("qro_allreduce", i, [i, i, i, i, vp, sz, vp, vp]),
+    ]:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB)
-        u16, u8, f32 = ctypes.c_uint16, ctypes.c_uint8, ctypes.c_float
-        sz, i = ctypes.c_size_t, ctypes.c_int
-        vp = ctypes.c_void_p
-        for name, res, args in [
-            ("qro_f16_to_f32", f32, [u16]),
-            ("qro_f32_to_f16", u16, [f32]),
-            ("qro_f32_to_f16_satfinite", u16, [f32]),
-            ("qro_bf16_to_f32", f32, [u16]),
-            ("qro_f32_to_bf16", u16, [f32]),
-            ("qro_e4m3_to_f32", f32, [u8]),
-            ("qro_f32_to_e4m3_satfinite", u8, [f32]),
-            ("qro_encoded_bytes", sz, [i, sz]),
-            ("qro_quantize", i, [i, i, vp, sz, vp]),
-            ("qro_dequantize", i, [i, i, vp, sz, vp]),
-            ("qro_allreduce", i, [i, i, i, i, vp, sz, vp, vp]),
-        ]:
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(_LIB))
     return _lib
 
 
@@ -92,7 +95,7 @@ def _as_u16(x: np.ndarray) -> np.ndarray:
 
 # ----- scalar conversions (vectorised by looping; small arrays only) -----
 
-def _vec(fn, arr, out_dtype):
+def _vec(fn, arr, out_dtype):  # noqa: D103
     return np.array([fn(v) for v in arr.tolist()], dtype=out_dtype)
 
 
@@ -175,3 +178,37 @@ def allreduce(dtype: int, fmt: int, stages: int, inputs, want_wire: bool = True)
     if wire is not None:
         wire = wire[:encoded_bytes(fmt, n)]
     return out[:n], wire
+
+
+class Oracle:
+    """The same API as this module over another build of the oracle source
+    (used by the tests that plant mistakes in a copy of qro.c and check that
+    the pins catch them)."""
+
+    F16, BF16 = F16, BF16
+    FP, Q8, Q6, Q4, FP8, Q8A, Q4A = FP, Q8, Q6, Q4, FP8, Q8A, Q4A
+    BLOCK = BLOCK
+
+    def __init__(self, so_path: str):
+        self._lib = _bind(ctypes.CDLL(so_path))
+
+    def __getattr__(self, name):
+        fn = globals().get(name)
+        if not callable(fn) or name.startswith("_") or name in ("build", "compile_source"):
+            raise AttributeError(name)
+
+        def call(*args, **kwargs):
+            global _lib
+            saved = _lib
+            _lib = self._lib
+            try:
+                return fn(*args, **kwargs)
+            finally:
+                _lib = saved
+        return call
+
+
+def compile_source(src_path: str, out_path: str) -> str:
+    """Compile a copy of the oracle source with the oracle's flags."""
+    subprocess.run(["gcc", *CFLAGS, "-I", _HERE, "-o", out_path, src_path, "-lm"], check=True)
+    return out_path

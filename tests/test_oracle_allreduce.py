@@ -199,3 +199,18 @@ def test_rejects_bad_arguments(oracle_mod):
         oracle_mod.allreduce(F16, Q8, 3, x)
     with pytest.raises(ValueError):
         oracle_mod.allreduce(F16, Q8, 2, x * 5)  # W = 10
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_signed_zeros_fp_path(oracle_mod, dtype):
+    """IEEE signs of zero: -0 + -0 = -0 and -0 + +0 = +0, and W=1 returns
+    the input bits; the accumulation starts from rank 0's value itself."""
+    z = np.zeros(16, np.float32)
+    neg = to_bits(-z, dtype)
+    pos = to_bits(z, dtype)
+    out, _ = oracle_mod.allreduce(dtype, FP, 1, [neg])
+    assert np.array_equal(out, neg)
+    out, _ = oracle_mod.allreduce(dtype, FP, 1, [neg, neg])
+    assert np.array_equal(out, neg)
+    out, _ = oracle_mod.allreduce(dtype, FP, 2, [neg, pos])
+    assert np.array_equal(out, pos)
