@@ -70,6 +70,14 @@ def bytes_alg(W: int, n: int, fmt: int, stages: int, wire: bool) -> int:
     return b
 
 
+def bytes_alg_staged(W: int, n: int, fmt: int) -> int:
+    """Algorithmic bytes of the staged (stage-1 materialised) two-stage
+    allreduce: encode W messages into the exchange buffer, the owners read it
+    back and write the payload, the payload is decoded to the output."""
+    c = encoded_bytes(fmt, n)
+    return (W + 1) * n * 2 + (2 * W + 2) * c
+
+
 def step_name(fmt: int, stages: int) -> str:
     return f"{FORMAT_NAMES[fmt]}-{stages}stage"
 
@@ -438,6 +446,21 @@ def run_ours(args):
             codec[FORMAT_NAMES[fmt]] = row
             del enc
 
+    # ---------------- staged two-stage path (stage-1 exchange materialised) ----------------
+    staged = {}
+    if not args.no_extras:
+        st1 = torch.empty(max(qr.qr_stage1_bytes(W, f, n) for f in (FP8, Q8, Q6, Q4)), dtype=torch.uint8,
+                          device=dev)
+        for fmt in (FP8, Q8, Q6, Q4):
+            t = per_call_seconds(lambda: qr.qr_allreduce_staged(W, wl.dtype, fmt, ins, n, out, wires[fmt], st1),
+                                 args.sweep_reps)
+            ba = bytes_alg_staged(W, n, fmt)
+            staged[FORMAT_NAMES[fmt]] = {"us": round(t * 1e6, 2),
+                                         "fused_us": per_format[step_name(fmt, 2)]["us"],
+                                         "hbm_GBps": round(ba / t / 1e9, 1),
+                                         "hbm_frac": round(ba / t / 1e9 / peak, 3)}
+        del st1
+
     # ---------------- the other workloads ----------------
     extra = {}
     if not args.no_extras:
@@ -461,6 +484,20 @@ def run_ours(args):
                                                "hbm_GBps": round(ba / t / 1e9, 1),
                                                "hbm_frac": round(ba / t / 1e9 / peak, 3)}
                 del wire
+            if key == 5:
+                st1 = torch.empty(qr.qr_stage1_bytes(w.W, Q8, w.n), dtype=torch.uint8, device=dev)
+                for fmt in (Q8, Q4):
+                    wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
+                    t = per_call_seconds(
+                        lambda: qr.qr_allreduce_staged(w.W, w.dtype, fmt, dins, w.n, o, wire, st1),
+                        args.sweep_reps)
+                    ba = bytes_alg_staged(w.W, w.n, fmt)
+                    res[f"{FORMAT_NAMES[fmt]}-2stage-staged"] = {"us": round(t * 1e6, 1),
+                                                                 "algbw_GBps": round(w.n * 2 / t / 1e9, 1),
+                                                                 "hbm_GBps": round(ba / t / 1e9, 1),
+                                                                 "hbm_frac": round(ba / t / 1e9 / peak, 3)}
+                    del wire
+                del st1
             extra[w.name] = res
             del dins, o
             torch.cuda.empty_cache()
@@ -493,7 +530,8 @@ def run_ours(args):
             "gpu_launches": K * len(STEP_CALLS),
             "clocks": clocks, "wall_ms_per_step_incl_flush": round(wall / K * 1e3, 3),
             "flush_ms_per_step": round(t_flush / K * 1e3, 4),
-            "sweep_W2_fp16": sweep, "codec_fp16_64MiB": codec, "workloads": extra,
+            "sweep_W2_fp16": sweep, "codec_fp16_64MiB": codec, "staged_W2_fp16_64MiB": staged,
+            "workloads": extra,
         }
         print(json.dumps(line), flush=True)
     dist_barrier()

@@ -140,6 +140,31 @@ qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages,
                                 const void *const *inputs, size_t n,
                                 void *out, void *wire, void *stream);
 
+/* Bytes of the stage-1 exchange buffer qr_allreduce_staged needs: W x W
+ * slots, slot (j, r) holding rank r's chunk for owner j, with
+ * chunk_nb = ceil(nb / W) blocks per owner, each slot an encoded
+ * sub-message of chunk_nb blocks (codes | scales | zps; FP: the values)
+ * padded to 16 bytes.  0 for an invalid W or format.  Host only. */
+size_t qr_stage1_bytes(int W, qr_format fmt, size_t n);
+
+/* The two-stage allreduce with its stage-1 exchange materialised, the
+ * three-kernel structure a real multi-GPU quick allreduce has ("2stage" of
+ * vLLM PR #18473): (1) each rank encodes its message and writes chunk j's
+ * blocks into owner j's slot of `stage1` (reduce-scatter); (2) each owner
+ * decodes its W slots, sums in rank order in binary32 and requantizes into
+ * `wire` (the all-gather payload, same layout as qr_allreduce_emulated's);
+ * (3) `wire` is decoded into `out`.  out and wire are bit-identical to
+ * qr_allreduce_emulated(W, dt, fmt, 2, ...); only the memory traffic and
+ * the number of launches differ.
+ *   stage1  device, qr_stage1_bytes(W, fmt, n) bytes, 16-byte aligned,
+ *           caller-owned scratch (contents on return: the stage-1 slots)
+ *   wire    device, qr_encoded_bytes(fmt, n) bytes, required
+ * All buffers 16-byte aligned; outputs must not overlap inputs or each
+ * other.  Asynchronous on `stream` (three launches). */
+qr_status qr_allreduce_staged(int W, qr_dtype dt, qr_format fmt,
+                              const void *const *inputs, size_t n, void *out,
+                              void *wire, void *stage1, void *stream);
+
 /* Messages of at most qr_direct_limit() elements per rank are processed by a
  * single-pass kernel with one memory round trip (lowest latency); longer ones
  * by the persistent bulk-copy pipeline (highest bandwidth).  Both compute

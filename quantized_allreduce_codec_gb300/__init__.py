@@ -26,7 +26,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqr.so")
 EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
            "qr_status_string", "qr_device_error", "qr_direct_limit", "qr_set_direct_limit",
-           "qr_selftest_wait_timeout")
+           "qr_selftest_wait_timeout", "qr_stage1_bytes", "qr_allreduce_staged")
 
 _lib = None
 _lock = threading.Lock()
@@ -68,6 +68,10 @@ def lib():
                 L.qr_direct_limit.argtypes = []
                 L.qr_set_direct_limit.restype = None
                 L.qr_set_direct_limit.argtypes = [sz]
+                L.qr_stage1_bytes.restype = sz
+                L.qr_stage1_bytes.argtypes = [i, i, sz]
+                L.qr_allreduce_staged.restype = i
+                L.qr_allreduce_staged.argtypes = [i, i, i, vp, sz, vp, vp, vp, vp]
                 L.qr_selftest_wait_timeout.restype = i
                 L.qr_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
                 _lib = L
@@ -161,3 +165,18 @@ def qr_set_direct_limit(n: int) -> None:
 def qr_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     """Launch the bounded-wait self-test (raises device flag 8 after limit_us)."""
     _check(lib().qr_selftest_wait_timeout(limit_us, _stream(stream)), "qr_selftest_wait_timeout")
+
+
+def qr_stage1_bytes(W: int, fmt: int, n: int) -> int:
+    """Bytes of the stage-1 exchange buffer of qr_allreduce_staged."""
+    return int(lib().qr_stage1_bytes(W, fmt, n))
+
+
+def qr_allreduce_staged(W: int, dtype, fmt: int, inputs, n: int, out, wire, stage1,
+                        stream=None) -> None:
+    """Two-stage allreduce with the stage-1 exchange materialised in `stage1`."""
+    ptrs = (ctypes.c_void_p * max(len(inputs), 1))(*[_addr(x) for x in inputs])
+    _check(lib().qr_allreduce_staged(W, _dtype_code(dtype), fmt,
+                                     ctypes.cast(ptrs, ctypes.c_void_p) if inputs else None, n,
+                                     _addr(out), _addr(wire), _addr(stage1), _stream(stream)),
+           "qr_allreduce_staged")

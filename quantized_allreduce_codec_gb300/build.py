@@ -33,7 +33,8 @@ def nvcc() -> str:
 
 
 def _sources():
-    return [os.path.join(CSRC, f) for f in ("qr_api.cu", "qr_kernels.cu", "qr_device.cuh", "qr_launch.h")] + \
+    return [os.path.join(CSRC, f) for f in ("qr_api.cu", "qr_kernels.cu", "qr_device.cuh", "qr_launch.h",
+                                             "qr_staged.cuh")] + \
         [os.path.join(INCLUDE, "qr.h")]
 
 

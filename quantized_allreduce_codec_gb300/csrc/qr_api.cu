@@ -86,6 +86,28 @@ cudaError_t dispatch_decode(int fmt, int dt, const DecodeParams& p, cudaStream_t
   }
 }
 
+cudaError_t dispatch_staged(int fmt, int dt, const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
+  switch (fmt) {
+    case 0: return launch_staged_fmt_0(dt, p, dp, s);
+    case 1: return launch_staged_fmt_1(dt, p, dp, s);
+    case 2: return launch_staged_fmt_2(dt, p, dp, s);
+    case 3: return launch_staged_fmt_3(dt, p, dp, s);
+    case 4: return launch_staged_fmt_4(dt, p, dp, s);
+    case 5: return launch_staged_fmt_5(dt, p, dp, s);
+    case 6: return launch_staged_fmt_6(dt, p, dp, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Stage-1 slot geometry: chunk_nb = ceil(nb / W) blocks per owner; a slot is
+// one encoded sub-message of chunk_nb blocks, padded to 16 bytes.
+void staged_geometry(int W, int fmt, size_t n, size_t* chunk_nb, size_t* slot_bytes) {
+  const size_t nb = (n + 31) / 32;
+  *chunk_nb = (nb + W - 1) / W;
+  size_t per_block = fmt == FMT_FP ? 64 : 32 * static_cast<size_t>(code_bits(fmt)) / 8 + 2 + (is_asym(fmt) ? 2 : 0);
+  *slot_bytes = (*chunk_nb * per_block + 15) / 16 * 16;
+}
+
 // Encoded layout: codes[nb][cb] | scales[nb] | zps[nb] (asymmetric only).
 void encoded_regions(int fmt, size_t n, void* base, uint8_t** codes, uint16_t** scales, uint16_t** zps,
                      uint16_t** fp_values) {
@@ -249,6 +271,64 @@ qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages, c
   if (!p.err) return QR_ERR_CUDA;
   const int mode = stages == 1 ? MODE_AR1 : MODE_AR2;
   return to_status(dispatch_pipeline(f, d, mode, p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t qr_stage1_bytes(int W, qr_format fmt, size_t n) {
+  const int f = static_cast<int>(fmt);
+  if ((W != 1 && W != 2 && W != 4 && W != 8) || !valid_format(f)) return 0;
+  size_t chunk_nb, slot_bytes;
+  staged_geometry(W, f, n, &chunk_nb, &slot_bytes);
+  return static_cast<size_t>(W) * W * slot_bytes;
+}
+
+qr_status qr_allreduce_staged(int W, qr_dtype dt, qr_format fmt, const void* const* inputs, size_t n, void* out,
+                              void* wire, void* stage1, void* stream) {
+  const int f = static_cast<int>(fmt), d = static_cast<int>(dt);
+  if (n && (!inputs || !out || !wire || !stage1)) return QR_ERR_NULL;
+  if (!valid_dtype(d)) return QR_ERR_DTYPE;
+  if (!valid_format(f)) return QR_ERR_FORMAT;
+  if (W != 1 && W != 2 && W != 4 && W != 8) return QR_ERR_WORLD;
+  qr_status st = check_size(n);
+  if (st != QR_OK) return st;
+  if (n == 0) return QR_OK;
+  for (int r = 0; r < W; ++r)
+    if (!inputs[r]) return QR_ERR_NULL;
+  if (!aligned16(out) || !aligned16(wire) || !aligned16(stage1)) return QR_ERR_ALIGN;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(inputs[r])) return QR_ERR_ALIGN;
+  const size_t msg = n * 2, wbytes = qr_encoded_bytes(fmt, n), sbytes = qr_stage1_bytes(W, fmt, n);
+  for (int r = 0; r < W; ++r)
+    if (overlap(inputs[r], msg, out, msg) || overlap(inputs[r], msg, wire, wbytes) ||
+        overlap(inputs[r], msg, stage1, sbytes))
+      return QR_ERR_OVERLAP;
+  if (overlap(out, msg, wire, wbytes) || overlap(out, msg, stage1, sbytes) || overlap(wire, wbytes, stage1, sbytes))
+    return QR_ERR_OVERLAP;
+
+  StagedParams p;
+  std::memset(&p, 0, sizeof p);
+  for (int r = 0; r < W; ++r) p.in[r] = inputs[r];
+  p.W = W;
+  p.n = n;
+  p.nb = (n + 31) / 32;
+  size_t chunk_nb, slot_bytes;
+  staged_geometry(W, f, n, &chunk_nb, &slot_bytes);
+  p.chunk_nb = chunk_nb;
+  p.slot_bytes = slot_bytes;
+  p.stage1 = static_cast<uint8_t*>(stage1);
+  encoded_regions(f, n, wire, &p.codes, &p.scales, &p.zps, &p.fp_values);
+
+  DecodeParams dp;
+  std::memset(&dp, 0, sizeof dp);
+  dp.codes = p.codes;
+  dp.scales = p.scales;
+  dp.zps = p.zps;
+  dp.fp_values = p.fp_values;
+  dp.out = out;
+  dp.n = n;
+  dp.nb = p.nb;
+  dp.err = device_error_word();
+  if (!dp.err) return QR_ERR_CUDA;
+  return to_status(dispatch_staged(f, d, p, dp, static_cast<cudaStream_t>(stream)));
 }
 
 size_t qr_direct_limit(void) { return static_cast<size_t>(g_direct_limit.load()); }

@@ -83,7 +83,38 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int F, int D>
+cudaError_t launch_stg(const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
+  static int sm_count[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (sm_count[dev] == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev] = sms;
+  }
+  const unsigned long long cap = (unsigned long long)sm_count[dev] * 16;
+  const unsigned long long want1 = (p.nb * 4 * p.W + kDirectThreads - 1) / kDirectThreads;
+  const unsigned long long want2 = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;
+  qr_scatter_encode_kernel<F, D><<<static_cast<unsigned>(want1 < cap ? want1 : cap), kDirectThreads, 0, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  qr_owner_reduce_kernel<F, D><<<static_cast<unsigned>(want2 < cap ? want2 : cap), kDirectThreads, 0, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_dec<F, D>(dp, s);
+}
+
 }  // namespace
+
+cudaError_t QR_CAT(launch_staged_fmt_, QR_FMT)(int dt, const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
+  constexpr int F = QR_FMT;
+  if (dt == DT_F16) return launch_stg<F, DT_F16>(p, dp, s);
+  return launch_stg<F, DT_BF16>(p, dp, s);
+}
 
 cudaError_t QR_CAT(launch_pipeline_fmt_, QR_FMT)(int dt, int mode, const PipeParams& p, cudaStream_t s) {
   constexpr int F = QR_FMT;

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "qr_device.cuh"
+#include "qr_staged.cuh"
 
 namespace qr {
 
@@ -15,7 +16,8 @@ namespace qr {
 #define QR_DECLARE_FMT(N)                                                                   \
   cudaError_t launch_pipeline_fmt_##N(int dt, int mode, const PipeParams& p, cudaStream_t s); \
   cudaError_t launch_direct_fmt_##N(int dt, int mode, const PipeParams& p, cudaStream_t s);   \
-  cudaError_t launch_decode_fmt_##N(int dt, const DecodeParams& p, cudaStream_t s);
+  cudaError_t launch_decode_fmt_##N(int dt, const DecodeParams& p, cudaStream_t s);            \
+  cudaError_t launch_staged_fmt_##N(int dt, const StagedParams& p, const DecodeParams& dp, cudaStream_t s);
 QR_DECLARE_FMT(0)
 QR_DECLARE_FMT(1)
 QR_DECLARE_FMT(2)

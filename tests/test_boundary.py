@@ -24,7 +24,7 @@ def L():
 def header_functions(path):
     text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(qr_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(qr_[a-z0-9_]+)\s*\(", text)))
 
 
 def header_enum(path, prefix):
@@ -144,3 +144,15 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(qr, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         qr.lib()
+
+
+def test_stage1_bytes_geometry(L):
+    # W x W slots of ceil(nb / W) blocks each, padded to 16 bytes
+    for W in (1, 2, 4, 8):
+        for fmt, per_block in ((1, 34), (2, 26), (3, 18), (4, 34), (5, 36), (6, 20), (0, 64)):
+            for n in (8, 40, 8200, 1 << 20):
+                nb = (n + 31) // 32
+                cnb = (nb + W - 1) // W
+                assert qr.qr_stage1_bytes(W, fmt, n) == W * W * ((cnb * per_block + 15) // 16 * 16)
+    assert qr.qr_stage1_bytes(3, 1, 64) == 0
+    assert qr.qr_stage1_bytes(2, 9, 64) == 0

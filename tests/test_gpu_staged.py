@@ -1,0 +1,120 @@
+"""GPU parity of the staged two-stage allreduce (stage-1 exchange
+materialised): output and payload bit-equal to the oracle's two-stage
+result, and every stage-1 slot bit-equal to the oracle's encoding of that
+rank's chunk for that owner."""
+import numpy as np
+import pytest
+import torch
+
+import quantized_allreduce_codec_gb300 as qr
+from quantized_allreduce_codec_gb300 import build
+from quantized_allreduce_codec_gb300.inputs import (ALL_FORMATS, BF16, F16, FP, Q4, Q4A, Q8,
+                                                    sweep_workload, to_bits)
+from qr_gpu_util import (CODE_BITS, dev_u16, guard_intact, out_buffer, sample_blocks,
+                         split_encoded)
+from test_gpu_parity import assert_bits_equal, assert_encoded_equal, spread_values
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    qr.lib()
+    qr.qr_device_error(clear=True)
+    yield
+    assert qr.qr_device_error(clear=True) == 0
+
+
+def run_staged(dtype, fmt, xs=None, dev_inputs=None):
+    ins = dev_inputs if dev_inputs is not None else [dev_u16(x) for x in xs]
+    W, n = len(ins), ins[0].numel()
+    wbytes, sbytes = qr.qr_encoded_bytes(fmt, n), qr.qr_stage1_bytes(W, fmt, n)
+    out, wire, st1 = out_buffer(2 * n), out_buffer(wbytes), out_buffer(sbytes)
+    qr.qr_allreduce_staged(W, dtype, fmt, ins, n, out, wire, st1)
+    torch.cuda.synchronize()
+    assert guard_intact(out, 2 * n) and guard_intact(wire, wbytes) and guard_intact(st1, sbytes)
+    return (out[:2 * n].cpu().numpy().view(np.uint16), wire[:wbytes].cpu().numpy(),
+            st1[:sbytes].cpu().numpy())
+
+
+def slot_geometry(W, fmt, n):
+    nb = (n + 31) // 32
+    cnb = (nb + W - 1) // W
+    per_block = 64 if fmt == FP else 32 * CODE_BITS[fmt] // 8 + (4 if fmt in (5, 6) else 2)
+    return nb, cnb, (cnb * per_block + 15) // 16 * 16
+
+
+def check_slots(oracle_mod, dtype, fmt, xs, st1):
+    W, n = len(xs), xs[0].size
+    nb, cnb, slot = slot_geometry(W, fmt, n)
+    assert st1.size == W * W * slot
+    for j in range(W):
+        b0, b1 = j * cnb, min(nb, (j + 1) * cnb)
+        if b0 >= b1:
+            continue
+        e0, e1 = 32 * b0, min(n, 32 * b1)
+        for r in range(W):
+            s = st1[(j * W + r) * slot:(j * W + r + 1) * slot]
+            chunk = xs[r][e0:e1]
+            if fmt == FP:
+                assert np.array_equal(s[:2 * (e1 - e0)].view(np.uint16), chunk)
+                continue
+            want = oracle_mod.quantize(dtype, fmt, chunk)
+            real = b1 - b0
+            gc, gs, gz = split_encoded(s, fmt, cnb * 32)
+            wc, ws, wz = split_encoded(want, fmt, e1 - e0)
+            assert np.array_equal(gc[:real], wc), (j, r)
+            assert np.array_equal(gs[:real], ws), (j, r)
+            if gz is not None:
+                assert np.array_equal(gz[:real], wz), (j, r)
+
+
+@pytest.mark.parametrize("n", [8, 40, 8200, 3 * 8192 + 40])
+@pytest.mark.parametrize("fmt", ALL_FORMATS)
+@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("W", [1, 2, 4, 8])
+def test_staged_parity(oracle_mod, W, dtype, fmt, n):
+    rng = np.random.default_rng(8000 + 7 * W + 13 * fmt + n)
+    xs = [spread_values(rng, n, dtype, zero_blocks=(r == 0)) for r in range(W)]
+    out, wire, st1 = run_staged(dtype, fmt, xs)
+    o_out, o_wire = oracle_mod.allreduce(dtype, fmt, 2, xs)
+    assert_bits_equal(out, o_out)
+    assert_encoded_equal(wire, o_wire, fmt, n)
+    check_slots(oracle_mod, dtype, fmt, xs, st1)
+
+
+@pytest.mark.parametrize("fmt", [FP, Q8, Q4, Q4A])
+def test_staged_equals_fused_at_64MiB(oracle_mod, fmt):
+    """tp2's largest message: staged and fused paths give the same bits
+    everywhere, and sampled blocks match the oracle."""
+    wl = sweep_workload(64 << 20)
+    xs = wl.inputs()
+    dev = [dev_u16(x) for x in xs]
+    out, wire, _ = run_staged(wl.dtype, fmt, dev_inputs=dev)
+    n = wl.n
+    fo, fw = out_buffer(2 * n), out_buffer(qr.qr_encoded_bytes(fmt, n))
+    qr.qr_allreduce_emulated(2, wl.dtype, fmt, 2, dev, n, fo, fw)
+    torch.cuda.synchronize()
+    assert_bits_equal(out, fo[:2 * n].cpu().numpy().view(np.uint16), "staged vs fused")
+    assert np.array_equal(wire, fw[:qr.qr_encoded_bytes(fmt, n)].cpu().numpy())
+    blocks = sample_blocks(n, 2000, 11 + fmt)
+    sub = [np.concatenate([x[32 * b:32 * b + 32] for b in blocks]) for x in xs]
+    o_out, _ = oracle_mod.allreduce(wl.dtype, fmt, 2, sub)
+    assert_bits_equal(np.concatenate([out[32 * b:32 * b + 32] for b in blocks]), o_out)
+
+
+def test_staged_argument_errors():
+    x = torch.zeros(64, dtype=torch.float16, device="cuda")
+    y = torch.zeros(64, dtype=torch.float16, device="cuda")
+    out = torch.empty_like(x)
+    wire = torch.empty(qr.qr_encoded_bytes(Q8, 64), dtype=torch.uint8, device="cuda")
+    st1 = torch.empty(qr.qr_stage1_bytes(2, Q8, 64), dtype=torch.uint8, device="cuda")
+    with pytest.raises(qr.QRError, match="QR_ERR_NULL"):
+        qr.qr_allreduce_staged(2, F16, Q8, [x, y], 64, out, None, st1)
+    with pytest.raises(qr.QRError, match="QR_ERR_OVERLAP"):
+        qr.qr_allreduce_staged(2, F16, Q8, [x, y], 64, out, wire, wire)
+    with pytest.raises(qr.QRError, match="QR_ERR_WORLD"):
+        qr.qr_allreduce_staged(3, F16, Q8, [x, y, y], 64, out, wire, st1)
+    assert qr.qr_stage1_bytes(3, Q8, 64) == 0
