@@ -87,7 +87,9 @@ typedef enum {
   QR_ERR_ALIGN = 7,   /* a pointer is not 16-byte aligned                     */
   QR_ERR_OVERLAP = 8, /* an output buffer overlaps an input or another output */
   QR_ERR_CUDA = 9,    /* the CUDA runtime reported an error                   */
-  QR_ERR_DEVICE = 10  /* a kernel gave up waiting (see qr_device_error)       */
+  QR_ERR_DEVICE = 10, /* a kernel gave up waiting (see qr_device_error)      */
+  QR_ERR_SCRATCH = 11 /* qr_allreduce_staged_noalloc: the message needs more
+                         stage-1 space than QR_NOALLOC_SCRATCH_BYTES         */
 } qr_status;
 
 /* Largest n accepted (elements per message): 2^36. */
@@ -164,6 +166,33 @@ size_t qr_stage1_bytes(int W, qr_format fmt, size_t n);
 qr_status qr_allreduce_staged(int W, qr_dtype dt, qr_format fmt,
                               const void *const *inputs, size_t n, void *out,
                               void *wire, void *stage1, void *stream);
+
+/* qr_allreduce_staged without the caller's stage-1 buffer, for callers that
+ * cannot allocate device memory: code that runs while a CUDA graph is being
+ * captured, a plugin or callback that only receives its input and output
+ * pointers and must not bypass its host framework's allocator, or a path
+ * where cudaMalloc/cudaFree (and cudaFree's device synchronisation) are not
+ * allowed.  The source pages have no counterpart: it exists for those
+ * callers.
+ *
+ * The stage-1 buffer is a fixed device array inside this library of
+ * QR_NOALLOC_SCRATCH_BYTES (16 MiB); every GPU on which the library is used
+ * keeps it until the process exits.  Messages whose qr_stage1_bytes(W, fmt,
+ * n) exceeds it are rejected with QR_ERR_SCRATCH (e.g. W=2 fp16 Q8 allows
+ * about 7.8M elements per rank).  Nothing is allocated by the call.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and keeps it; make that first call before any
+ * stream capture.  All calls share the one array: two calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race on
+ * it and their results are undefined; calls ordered on one stream are fine.
+ * Nothing in the array needs to start at zero: stage 1 writes every byte the
+ * owners read, whatever a previous call left there.
+ * Arguments, results and other errors as qr_allreduce_staged. */
+#define QR_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+qr_status qr_allreduce_staged_noalloc(int W, qr_dtype dt, qr_format fmt,
+                                      const void *const *inputs, size_t n,
+                                      void *out, void *wire, void *stream);
 
 /* Messages of at most qr_direct_limit() elements per rank are processed by a
  * single-pass kernel with one memory round trip (lowest latency); longer ones

@@ -20,13 +20,14 @@ FORMATS = {"FP": QR_FP, "Q8": QR_Q8, "Q6": QR_Q6, "Q4": QR_Q4, "FP8": QR_FP8,
            "Q8A": QR_Q8_ASYM, "Q4A": QR_Q4_ASYM}
 STATUS = ["QR_OK", "QR_ERR_NULL", "QR_ERR_DTYPE", "QR_ERR_FORMAT", "QR_ERR_WORLD",
           "QR_ERR_STAGES", "QR_ERR_SIZE", "QR_ERR_ALIGN", "QR_ERR_OVERLAP", "QR_ERR_CUDA",
-          "QR_ERR_DEVICE"]
+          "QR_ERR_DEVICE", "QR_ERR_SCRATCH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqr.so")
 EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
            "qr_status_string", "qr_device_error", "qr_direct_limit", "qr_set_direct_limit",
-           "qr_selftest_wait_timeout", "qr_stage1_bytes", "qr_allreduce_staged")
+           "qr_selftest_wait_timeout", "qr_stage1_bytes", "qr_allreduce_staged",
+           "qr_allreduce_staged_noalloc")
 
 _lib = None
 _lock = threading.Lock()
@@ -72,6 +73,8 @@ def lib():
                 L.qr_stage1_bytes.argtypes = [i, i, sz]
                 L.qr_allreduce_staged.restype = i
                 L.qr_allreduce_staged.argtypes = [i, i, i, vp, sz, vp, vp, vp, vp]
+                L.qr_allreduce_staged_noalloc.restype = i
+                L.qr_allreduce_staged_noalloc.argtypes = [i, i, i, vp, sz, vp, vp, vp]
                 L.qr_selftest_wait_timeout.restype = i
                 L.qr_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
                 _lib = L
@@ -180,3 +183,20 @@ def qr_allreduce_staged(W: int, dtype, fmt: int, inputs, n: int, out, wire, stag
                                      ctypes.cast(ptrs, ctypes.c_void_p) if inputs else None, n,
                                      _addr(out), _addr(wire), _addr(stage1), _stream(stream)),
            "qr_allreduce_staged")
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def qr_allreduce_staged_noalloc(W: int, dtype, fmt: int, inputs, n: int, out, wire,
+                                stream=None) -> None:
+    """qr_allreduce_staged with the library's built-in stage-1 array instead
+    of a caller buffer, for callers that cannot allocate device memory (for
+    example while a CUDA graph is being captured).  Messages needing more
+    than NOALLOC_SCRATCH_BYTES of stage-1 space raise QR_ERR_SCRATCH; calls
+    that overlap on the GPU share the array and race."""
+    ptrs = (ctypes.c_void_p * max(len(inputs), 1))(*[_addr(x) for x in inputs])
+    _check(lib().qr_allreduce_staged_noalloc(W, _dtype_code(dtype), fmt,
+                                             ctypes.cast(ptrs, ctypes.c_void_p) if inputs else None, n,
+                                             _addr(out), _addr(wire), _stream(stream)),
+           "qr_allreduce_staged_noalloc")

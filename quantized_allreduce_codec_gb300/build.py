@@ -34,7 +34,7 @@ def nvcc() -> str:
 
 def _sources():
     return [os.path.join(CSRC, f) for f in ("qr_api.cu", "qr_kernels.cu", "qr_device.cuh", "qr_launch.h",
-                                             "qr_staged.cuh")] + \
+                                             "qr_staged.cuh", "qr_noalloc.cu")] + \
         [os.path.join(INCLUDE, "qr.h")]
 
 
@@ -60,7 +60,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    jobs = [(os.path.join(CSRC, "qr_api.cu"), os.path.join(BUILD, "qr_api.o"), [], verbose)]
+    jobs = [(os.path.join(CSRC, "qr_api.cu"), os.path.join(BUILD, "qr_api.o"), [], verbose),
+            (os.path.join(CSRC, "qr_noalloc.cu"), os.path.join(BUILD, "qr_noalloc.o"), [], verbose)]
     for f in range(NUM_FORMATS):
         jobs.append((os.path.join(CSRC, "qr_kernels.cu"), os.path.join(BUILD, f"qr_kernels_f{f}.o"),
                      [f"-DQR_FMT={f}"], verbose))

@@ -180,6 +180,7 @@ const char* qr_status_string(qr_status st) {
     case QR_ERR_OVERLAP: return "an output buffer overlaps an input or another output";
     case QR_ERR_CUDA: return "CUDA runtime error";
     case QR_ERR_DEVICE: return "a kernel gave up waiting on its pipeline";
+    case QR_ERR_SCRATCH: return "the message needs more stage-1 space than the built-in scratch array holds";
     default: return "unknown status";
   }
 }
