@@ -43,7 +43,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from quantized_allreduce_codec_gb300.inputs import (BF16, F16, FORMAT_NAMES, FP, FP8, Q4,  # noqa: E402
-                                                    Q4A, Q6, Q8, Q8A, sweep_sizes_bytes,
+                                                    Q4A, Q6, Q8, Q8A, from_bits, sweep_sizes_bytes,
                                                     sweep_workload, workloads)
 
 METRIC = "emulated quick-allreduce GB/s per rank-message and % of HBM roofline, 1×GB300"
@@ -484,6 +484,28 @@ def run_ours(args):
                                                "hbm_GBps": round(ba / t / 1e9, 1),
                                                "hbm_frac": round(ba / t / 1e9 / peak, 3)}
                 del wire
+            if key in (3, 4):
+                # the bf16 -> fp16 cast option against native bf16: speed, and
+                # error against the exact sum on 4096 sampled blocks
+                host_w = [w.rank_bits(r) for r in range(w.W)]
+                rng = np.random.default_rng(key)
+                blocks = np.sort(rng.choice(w.n // 32, 4096, replace=False))
+                idx = (blocks[:, None] * 32 + np.arange(32)[None, :]).reshape(-1)
+                exact = sum(from_bits(h[idx], BF16).astype(np.float64) for h in host_w)
+                for fmt in w.formats:
+                    wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
+                    row = {}
+                    for tag, dt in (("native_bf16", BF16), ("cast_via_fp16", 2)):
+                        t = per_call_seconds(
+                            lambda: qr.qr_allreduce_emulated(w.W, dt, fmt, 2, dins, w.n, o, wire, None),
+                            args.sweep_reps)
+                        got = from_bits(o.cpu().numpy().view(np.uint16)[idx], BF16).astype(np.float64)
+                        err = np.abs(got - exact)
+                        row[tag] = {"us": round(t * 1e6, 1), "max_abs_err": float(err.max()),
+                                    "mean_abs_err": float(err.mean()),
+                                    "inf_outputs": int(np.isinf(got).sum())}
+                    res[f"{FORMAT_NAMES[fmt]}-2stage-cast-option"] = row
+                    del wire
             if key == 5:
                 st1 = torch.empty(qr.qr_stage1_bytes(w.W, Q8, w.n), dtype=torch.uint8, device=dev)
                 for fmt in (Q8, Q4):

@@ -65,8 +65,14 @@
 extern "C" {
 #endif
 
-/* Message dtypes (_SUPPORTED_DTYPES on the quick_all_reduce API page). */
-typedef enum { QR_F16 = 0, QR_BF16 = 1 } qr_dtype;
+/* Message dtypes (_SUPPORTED_DTYPES on the quick_all_reduce API page).
+ * QR_BF16_AS_F16 (qr_allreduce_emulated only): bf16 messages, processed the
+ * way the bf16 -> fp16 cast option of init_quick_all_reduce on that page
+ * describes -- each input rounded to fp16 (nearest even; values beyond
+ * +-65504 become infinities, outside the contract), the fp16 allreduce run,
+ * its fp16 result rounded to bf16 for `out`; the payload in `wire` is the
+ * fp16 run's.  The other entry points reject it with QR_ERR_DTYPE. */
+typedef enum { QR_F16 = 0, QR_BF16 = 1, QR_BF16_AS_F16 = 2 } qr_dtype;
 
 /* Formats.  0..3 are QuickReduceRegime's values (FP, INT8, INT6, INT4) from
  * the quick_all_reduce API page; 4 is the "2stage f8" format of vLLM PR

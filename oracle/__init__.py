@@ -30,7 +30,7 @@ _lib = None
 
 # Values repeated from qro.h (0..3 follow QuickReduceRegime on the vLLM
 # quick_all_reduce API page; 4..6 are fp8 and the asymmetric formats).
-F16, BF16 = 0, 1
+F16, BF16, BF16_AS_F16 = 0, 1, 2
 FP, Q8, Q6, Q4, FP8, Q8A, Q4A = 0, 1, 2, 3, 4, 5, 6
 BLOCK = 32
 
@@ -185,7 +185,7 @@ class Oracle:
     (used by the tests that plant mistakes in a copy of qro.c and check that
     the pins catch them)."""
 
-    F16, BF16 = F16, BF16
+    F16, BF16, BF16_AS_F16 = F16, BF16, BF16_AS_F16
     FP, Q8, Q6, Q4, FP8, Q8A, Q4A = FP, Q8, Q6, Q4, FP8, Q8A, Q4A
     BLOCK = BLOCK
 

@@ -15,6 +15,7 @@
 #include "qro.h"
 
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ------------------------------------------------------------------------ */
@@ -355,9 +356,13 @@ int qro_dequantize(int dtype, int fmt, const uint8_t *enc, size_t n, uint16_t *o
  *      d(acc), so yhat = d(acc) and the payload is d(acc).
  *      stages == 1: yhat = acc.
  *   5. out = d(yhat): the same on every rank, so one copy is produced. */
+static int allreduce_cast_bf16_via_f16(int W, int fmt, int stages, const uint16_t *const *inputs, size_t n,
+                                       uint16_t *out, uint8_t *wire);
+
 int qro_allreduce(int W, int dtype, int fmt, int stages,
                   const uint16_t *const *inputs, size_t n,
                   uint16_t *out, uint8_t *wire) {
+  if (dtype == QRO_BF16_AS_F16) return allreduce_cast_bf16_via_f16(W, fmt, stages, inputs, n, out, wire);
   if (W < 1 || W > 8 || !valid_dtype(dtype) || !valid_format(fmt)) return -1;
   if (stages != 1 && stages != 2) return -1;
   if (n && (!inputs || !out)) return -1;
@@ -405,4 +410,30 @@ int qro_allreduce(int W, int dtype, int fmt, int stages,
     }
   }
   return 0;
+}
+
+/* The bf16 -> fp16 cast option: round each bf16 input to fp16 (nearest even,
+ * overflow to infinity), run the fp16 allreduce, round its fp16 result to
+ * bf16.  Scratch copies come from the heap; this is test code. */
+
+static int allreduce_cast_bf16_via_f16(int W, int fmt, int stages, const uint16_t *const *inputs, size_t n,
+                                       uint16_t *out, uint8_t *wire) {
+  if (W < 1 || W > 8 || !valid_format(fmt) || (stages != 1 && stages != 2)) return -1;
+  if (n == 0) return 0;
+  if (!inputs || !out) return -1;
+  uint16_t *buf = (uint16_t *)malloc(sizeof(uint16_t) * n * (size_t)(W + 1));
+  if (!buf) return -1;
+  const uint16_t *h[8];
+  for (int r = 0; r < W; ++r) {
+    if (!inputs[r]) { free(buf); return -1; }
+    uint16_t *dst = buf + (size_t)r * n;
+    for (size_t i = 0; i < n; ++i) dst[i] = qro_f32_to_f16(qro_bf16_to_f32(inputs[r][i]));
+    h[r] = dst;
+  }
+  uint16_t *o16 = buf + (size_t)W * n;
+  int rc = qro_allreduce(W, QRO_F16, fmt, stages, h, n, o16, wire);
+  if (rc == 0)
+    for (size_t i = 0; i < n; ++i) out[i] = qro_f32_to_bf16(qro_f16_to_f32(o16[i]));
+  free(buf);
+  return rc;
 }

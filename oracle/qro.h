@@ -40,7 +40,7 @@ extern "C" {
  * library); a test checks that both sides agree.  0..3 follow
  * QuickReduceRegime on [P4]; 4..6 are the fp8 format of [P1] and the
  * asymmetric formats of [P2]. */
-enum { QRO_F16 = 0, QRO_BF16 = 1 };
+enum { QRO_F16 = 0, QRO_BF16 = 1, QRO_BF16_AS_F16 = 2 };
 enum {
   QRO_FP = 0, QRO_Q8 = 1, QRO_Q6 = 2, QRO_Q4 = 3,
   QRO_FP8 = 4, QRO_Q8A = 5, QRO_Q4A = 6
@@ -66,7 +66,11 @@ int qro_quantize(int dtype, int fmt, const uint16_t *in, size_t n, uint8_t *enc)
 int qro_dequantize(int dtype, int fmt, const uint8_t *enc, size_t n, uint16_t *out);
 
 /* Emulated allreduce of W messages of n elements each (out-of-place).
- * wire (may be NULL) receives the stage-2 payload for stages == 2. */
+ * wire (may be NULL) receives the stage-2 payload for stages == 2.
+ * dtype QRO_BF16_AS_F16: bf16 messages are rounded to fp16 first, the fp16
+ * allreduce runs, and its result is rounded back to bf16 (the bf16 -> fp16
+ * cast option of init_quick_all_reduce on the vLLM quick_all_reduce page);
+ * the payload is the fp16 run's. */
 int qro_allreduce(int W, int dtype, int fmt, int stages,
                   const uint16_t *const *inputs, size_t n,
                   uint16_t *out, uint8_t *wire);

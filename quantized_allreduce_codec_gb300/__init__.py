@@ -14,7 +14,7 @@ import ctypes
 import os
 import threading
 
-F16, BF16 = 0, 1
+F16, BF16, BF16_AS_F16 = 0, 1, 2
 QR_FP, QR_Q8, QR_Q6, QR_Q4, QR_FP8, QR_Q8_ASYM, QR_Q4_ASYM = 0, 1, 2, 3, 4, 5, 6
 FORMATS = {"FP": QR_FP, "Q8": QR_Q8, "Q6": QR_Q6, "Q4": QR_Q4, "FP8": QR_FP8,
            "Q8A": QR_Q8_ASYM, "Q4A": QR_Q4_ASYM}

@@ -241,7 +241,7 @@ qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages, c
                                 size_t n, void* out, void* wire, void* stream) {
   const int f = static_cast<int>(fmt), d = static_cast<int>(dt);
   if (n && (!inputs || !out)) return QR_ERR_NULL;
-  if (!valid_dtype(d)) return QR_ERR_DTYPE;
+  if (!valid_dtype(d) && d != DT_BF16_AS_F16) return QR_ERR_DTYPE;
   if (!valid_format(f)) return QR_ERR_FORMAT;
   if (W != 1 && W != 2 && W != 4 && W != 8) return QR_ERR_WORLD;
   if (stages != 1 && stages != 2) return QR_ERR_STAGES;

@@ -118,6 +118,11 @@ cudaError_t QR_CAT(launch_staged_fmt_, QR_FMT)(int dt, const StagedParams& p, co
 
 cudaError_t QR_CAT(launch_pipeline_fmt_, QR_FMT)(int dt, int mode, const PipeParams& p, cudaStream_t s) {
   constexpr int F = QR_FMT;
+  if (dt == DT_BF16_AS_F16) {  // allreduce modes only
+    if (mode == MODE_AR1) return launch_pipe<F, DT_BF16_AS_F16, MODE_AR1>(p, s);
+    if (mode == MODE_AR2) return launch_pipe<F, DT_BF16_AS_F16, MODE_AR2>(p, s);
+    return cudaErrorInvalidValue;
+  }
   if (dt == DT_F16) {
     if (mode == MODE_ENCODE) return launch_pipe<F, DT_F16, MODE_ENCODE>(p, s);
     if (mode == MODE_AR1) return launch_pipe<F, DT_F16, MODE_AR1>(p, s);
@@ -130,6 +135,11 @@ cudaError_t QR_CAT(launch_pipeline_fmt_, QR_FMT)(int dt, int mode, const PipePar
 
 cudaError_t QR_CAT(launch_direct_fmt_, QR_FMT)(int dt, int mode, const PipeParams& p, cudaStream_t s) {
   constexpr int F = QR_FMT;
+  if (dt == DT_BF16_AS_F16) {  // allreduce modes only
+    if (mode == MODE_AR1) return launch_dir<F, DT_BF16_AS_F16, MODE_AR1>(p, s);
+    if (mode == MODE_AR2) return launch_dir<F, DT_BF16_AS_F16, MODE_AR2>(p, s);
+    return cudaErrorInvalidValue;
+  }
   if (dt == DT_F16) {
     if (mode == MODE_ENCODE) return launch_dir<F, DT_F16, MODE_ENCODE>(p, s);
     if (mode == MODE_AR1) return launch_dir<F, DT_F16, MODE_AR1>(p, s);

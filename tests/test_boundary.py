@@ -55,6 +55,7 @@ def test_enums_agree_with_oracle_and_page():
     assert lib_fmt["QR_Q8_ASYM"] == orc["QRO_Q8A"]
     assert lib_fmt["QR_Q4_ASYM"] == orc["QRO_Q4A"]
     assert lib_fmt["QR_F16"] == orc["QRO_F16"] and lib_fmt["QR_BF16"] == orc["QRO_BF16"]
+    assert lib_fmt["QR_BF16_AS_F16"] == orc["QRO_BF16_AS_F16"]
     for name, v in lib_fmt.items():
         if name.startswith("QR_ERR") or name == "QR_OK":
             assert qr.STATUS[v] == name
@@ -107,7 +108,7 @@ def test_allreduce_argument_errors(L):
     assert _ar(2, 0, 1, 2, ok_in, 0, None) == 0                      # empty message: nothing to do
     assert _ar(2, 0, 1, 2, ok_in, 64, None) == 1                     # QR_ERR_NULL
     assert _ar(2, 0, 1, 2, [A, 0], 64, C) == 1                       # NULL rank pointer
-    assert _ar(2, 2, 1, 2, ok_in, 64, C) == 2                        # QR_ERR_DTYPE
+    assert _ar(2, 3, 1, 2, ok_in, 64, C) == 2                        # QR_ERR_DTYPE
     assert _ar(2, 0, 7, 2, ok_in, 64, C) == 3                        # QR_ERR_FORMAT
     assert _ar(3, 0, 1, 2, [A, B, A], 64, C) == 4                    # QR_ERR_WORLD
     assert _ar(16, 0, 1, 2, ok_in * 8, 64, C) == 4
@@ -135,6 +136,8 @@ def test_codec_argument_errors(L):
     assert d(0, 1, A, 64, None, None) == 1
     assert d(1, 4, A, 64, A + 32, None) == 8
     assert d(0, 2, A, 64, B + 2, None) == 7
+    assert q(2, 1, A, 64, B, None) == 2                               # cast option: allreduce only
+    assert d(2, 1, A, 64, B, None) == 2
     assert qr.lib().qr_selftest_wait_timeout(0, None) == 6           # limit out of range
     assert qr.lib().qr_selftest_wait_timeout(1000001, None) == 6
 

@@ -13,7 +13,8 @@ import torch
 import quantized_allreduce_codec_gb300 as qr
 from quantized_allreduce_codec_gb300 import build
 from quantized_allreduce_codec_gb300.inputs import (ALL_FORMATS, BF16, F16, FP, FP8, Q4, Q4A, Q6,
-                                                    Q8, Q8A, sweep_workload, to_bits, workloads)
+                                                    Q8, Q8A, from_bits, sweep_workload, to_bits,
+                                                    workloads)
 from qr_gpu_util import (dev_u16, gather_blocks, gpu_allreduce, gpu_dequantize, gpu_quantize,
                          out_buffer, sample_blocks, split_encoded)
 
@@ -311,3 +312,22 @@ def test_direct_limit_default_and_paths_agree(oracle_mod):
             assert np.array_equal(wa, wb)
     finally:
         qr.qr_set_direct_limit(old)
+
+
+@pytest.mark.parametrize("n", [40, 8200, 3 * 8192 + 40])
+@pytest.mark.parametrize("stages", [1, 2])
+@pytest.mark.parametrize("fmt", ALL_FORMATS)
+@pytest.mark.parametrize("W", [1, 2, 8])
+def test_bf16_cast_option_parity(oracle_mod, W, fmt, stages, n, path):
+    """bf16 messages through the fp16 path (the cast option), inside the fp16
+    range, against the oracle's reading of the option."""
+    rng = np.random.default_rng(9500 + 7 * W + 13 * fmt + n + stages)
+    xs = []
+    for r in range(W):
+        v = from_bits(spread_values(rng, n, F16, zero_blocks=(r == 0)), F16)
+        xs.append(to_bits(v, BF16))
+    out, wire = gpu_allreduce(qr.BF16_AS_F16, fmt, stages, xs)
+    o_out, o_wire = oracle_mod.allreduce(qr.BF16_AS_F16, fmt, stages, xs)
+    assert_bits_equal(out, o_out)
+    if stages == 2:
+        assert_encoded_equal(wire, o_wire, fmt, n)

@@ -214,3 +214,20 @@ def test_signed_zeros_fp_path(oracle_mod, dtype):
     assert np.array_equal(out, neg)
     out, _ = oracle_mod.allreduce(dtype, FP, 2, [neg, pos])
     assert np.array_equal(out, pos)
+
+
+@pytest.mark.parametrize("fmt", ALL_FORMATS)
+@pytest.mark.parametrize("stages", [1, 2])
+def test_bf16_cast_option_is_fp16_run_between_library_casts(oracle_mod, fmt, stages):
+    """The bf16 -> fp16 cast option equals: round the bf16 messages to fp16
+    with numpy, run the fp16 allreduce, round the result to bf16 with torch."""
+    rng = np.random.default_rng(90 + fmt + stages)
+    W, n = 4, 32 * 40 + 8
+    xb = ranks(rng, W, n, BF16, 3.0)
+    as16 = [from_bits(x, BF16).astype(np.float16).view(np.uint16) for x in xb]
+    o16, w16 = oracle_mod.allreduce(F16, fmt, stages, as16)
+    want = cast(from_bits(o16, F16), BF16)
+    out, wire = oracle_mod.allreduce(2, fmt, stages, xb)
+    assert np.array_equal(out, want)
+    if stages == 2:
+        assert np.array_equal(wire, w16)
