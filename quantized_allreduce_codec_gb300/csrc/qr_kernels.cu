@@ -96,13 +96,13 @@ cudaError_t launch_stg(const StagedParams& p, const DecodeParams& dp, cudaStream
     if (e != cudaSuccess) return e;
     sm_count[dev] = sms;
   }
-  const unsigned long long cap = (unsigned long long)sm_count[dev] * 16;
-  const unsigned long long want1 = (p.nb * 4 * p.W + kDirectThreads - 1) / kDirectThreads;
-  const unsigned long long want2 = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;
-  qr_scatter_encode_kernel<F, D><<<static_cast<unsigned>(want1 < cap ? want1 : cap), kDirectThreads, 0, s>>>(p);
+  const unsigned long long cap = (unsigned long long)sm_count[dev] * 8;
+  const unsigned long long want = (p.nb + kStagedThreads - 1) / kStagedThreads;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  qr_scatter_encode_kernel<F, D><<<grid, kStagedThreads, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  qr_owner_reduce_kernel<F, D><<<static_cast<unsigned>(want2 < cap ? want2 : cap), kDirectThreads, 0, s>>>(p);
+  qr_owner_reduce_kernel<F, D><<<grid, kStagedThreads, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_dec<F, D>(dp, s);

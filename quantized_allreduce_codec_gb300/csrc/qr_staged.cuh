@@ -47,115 +47,233 @@ __device__ __forceinline__ unsigned long long slot_zps_off(unsigned long long ch
   return chunk_nb * (FmtInfo<F>::code_bytes + 2);
 }
 
-// Kernel 1: one thread per (rank, 8-element chunk); four lanes per block.
-template <int F, int D>
-__global__ void __launch_bounds__(kDirectThreads) qr_scatter_encode_kernel(const __grid_constant__ StagedParams p) {
-  const int lane = threadIdx.x & 31;
-  const unsigned long long per_rank = p.nb * 4;  // chunk slots per rank (padded final block)
-  const unsigned long long total = per_rank * p.W;
-  const unsigned long long nchunks = p.n / 8;
-  const unsigned long long stride = (unsigned long long)gridDim.x * kDirectThreads;
-  for (unsigned long long base = (unsigned long long)blockIdx.x * kDirectThreads + (threadIdx.x & ~31u);
-       base < total; base += stride) {
-    const unsigned long long idx = base + lane;
-    const bool live = idx < total;
-    const int r = live ? static_cast<int>(idx / per_rank) : 0;
-    const unsigned long long g = live ? idx - static_cast<unsigned long long>(r) * per_rank : 0;
-    const bool valid = live && g < nchunks;
-    const unsigned long long blk = g >> 2;
-    const int c = static_cast<int>(g & 3);
-    const unsigned long long j = blk / p.chunk_nb;
-    const unsigned long long local = blk - j * p.chunk_nb;
-    uint8_t* slot = p.stage1 + (j * p.W + r) * p.slot_bytes;
+// Owner of block blk: the number of owner starts k*chunk_nb (k >= 1) at or
+// below it (W - 1 comparisons; no division).
+__device__ __forceinline__ unsigned long long owner_of(unsigned long long blk, unsigned long long chunk_nb, int W) {
+  unsigned long long j = 0;
+#pragma unroll
+  for (int k = 1; k < 8; ++k)
+    if (k < W && blk >= static_cast<unsigned long long>(k) * chunk_nb) ++j;
+  return j;
+}
 
-    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-    if (valid) raw = reinterpret_cast<const uint4*>(p.in[r])[g];
-    if constexpr (!FmtInfo<F>::quant) {
-      if (valid) reinterpret_cast<uint4*>(slot + local * 64)[c] = raw;
-    } else {
-      bool fast;
-      const BlockScale b = group_scale_raw<F, D>(raw, valid, fast);
-      float x[8], dec[8];
-      uint32_t packed[2] = {0u, 0u};
-      widen8<D>(raw, x);
-      if (fast)
-        encode8<F, true>(x, b, dec, packed);
-      else
-        encode8<F, false>(x, b, dec, packed);
-      if (!valid) packed[0] = packed[1] = 0u;  // pad codes are 0
-      if (live) store_chunk_codes<F>(slot, local, c, packed);
-      if (live && c == 0) {
-        reinterpret_cast<uint16_t*>(slot + slot_scales_off<F>(p.chunk_nb))[local] = b.s_bits;
-        if (FmtInfo<F>::asym) reinterpret_cast<uint16_t*>(slot + slot_zps_off<F>(p.chunk_nb))[local] = b.z_bits;
+constexpr int kStagedThreads = 256;
+
+// Block scale and clamp-free flag of one block held as raw 16-bit words
+// (invalid chunks zeroed), as in the pipeline kernel's stage 1.
+template <int F, int D>
+__device__ __forceinline__ BlockScale raw_block_scale(const uint4 (&raw)[4], int nvalid, bool& fast) {
+  if (FmtInfo<F>::asym) {
+    float m, M;
+    raw_minmax<D>(raw, 0, nvalid, m, M);
+    const BlockScale b = scale_from_minmax<F>(m, M);
+    fast = clamp_free<F>(b, m, M);
+    return b;
+  }
+  const float a = raw_absmax<D>(raw);
+  const BlockScale b = scale_from_absmax<F>(a);
+  fast = FmtInfo<F>::fp8 ? true : clamp_free<F>(b, 0.0f, a);
+  return b;
+}
+
+template <int F>
+__device__ __forceinline__ BlockScale f32_block_scale(const float (&x)[32], int nvalid, bool& fast) {
+  if (FmtInfo<F>::asym) {
+    float m, M;
+    f32_minmax(x, 0, nvalid, m, M);
+    const BlockScale b = scale_from_minmax<F>(m, M);
+    fast = clamp_free<F>(b, m, M);
+    return b;
+  }
+  const float a = f32_absmax(x);
+  const BlockScale b = scale_from_absmax<F>(a);
+  fast = FmtInfo<F>::fp8 ? true : clamp_free<F>(b, 0.0f, a);
+  return b;
+}
+
+// Encode the four chunks of a block and store codes / scale / zero-point into
+// an encoded region (codes at codes + blk*cb, scale at scales[blk]).  The
+// block's code bytes are assembled in registers and written with the widest
+// aligned stores (32 B: two 16-byte stores; 16 B: one; Q6's 24 B: three
+// 8-byte stores).
+template <int F>
+__device__ __forceinline__ void encode_store_block(const float (&x)[32], const BlockScale& b, bool fast, int nvalid,
+                                                   uint8_t* codes, uint16_t* scales, uint16_t* zps,
+                                                   unsigned long long blk) {
+  uint32_t pk[4][2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float dec[8];
+    pk[k][0] = pk[k][1] = 0u;
+    if (fast)
+      encode8<F, true>(&x[8 * k], b, dec, pk[k]);
+    else
+      encode8<F, false>(&x[8 * k], b, dec, pk[k]);
+    if (FmtInfo<F>::asym && k >= nvalid) pk[k][0] = pk[k][1] = 0u;  // pad codes are 0
+  }
+  uint8_t* cp = codes + blk * FmtInfo<F>::code_bytes;
+  if (FmtInfo<F>::bits == 8) {
+    reinterpret_cast<uint4*>(cp)[0] = make_uint4(pk[0][0], pk[0][1], pk[1][0], pk[1][1]);
+    reinterpret_cast<uint4*>(cp)[1] = make_uint4(pk[2][0], pk[2][1], pk[3][0], pk[3][1]);
+  } else if (FmtInfo<F>::bits == 4) {
+    reinterpret_cast<uint4*>(cp)[0] = make_uint4(pk[0][0], pk[1][0], pk[2][0], pk[3][0]);
+  } else {  // four 48-bit pieces -> 192-bit little-endian stream
+    const uint32_t w0 = pk[0][0], w1 = (pk[0][1] & 0xFFFFu) | (pk[1][0] << 16);
+    const uint32_t w2 = (pk[1][0] >> 16) | (pk[1][1] << 16), w3 = pk[2][0];
+    const uint32_t w4 = (pk[2][1] & 0xFFFFu) | (pk[3][0] << 16), w5 = (pk[3][0] >> 16) | (pk[3][1] << 16);
+    uint2* c2 = reinterpret_cast<uint2*>(cp);  // 8-byte aligned: blk*24
+    c2[0] = make_uint2(w0, w1);
+    c2[1] = make_uint2(w2, w3);
+    c2[2] = make_uint2(w4, w5);
+  }
+  scales[blk] = b.s_bits;
+  if (FmtInfo<F>::asym) zps[blk] = b.z_bits;
+}
+
+// Kernel 1: one thread per block; for every rank, load its 64 bytes, encode
+// the block and write it into slot (owner, rank).
+template <int F, int D>
+__global__ void __launch_bounds__(kStagedThreads) qr_scatter_encode_kernel(const __grid_constant__ StagedParams p) {
+  const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
+  const int W = p.W;
+  for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
+       blk += stride) {
+    const unsigned long long rem = p.n - blk * 32;
+    const int nvalid = rem >= 32 ? 4 : static_cast<int>(rem / 8);
+    const unsigned long long j = owner_of(blk, p.chunk_nb, W);
+    const unsigned long long local = blk - j * p.chunk_nb;
+    uint4 next[4];  // the next rank's block, loaded one rank ahead
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      next[k] = k < nvalid ? __ldg(reinterpret_cast<const uint4*>(p.in[0]) + blk * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+    for (int r = 0; r < W; ++r) {
+      uint8_t* slot = p.stage1 + (j * W + r) * p.slot_bytes;
+      uint4 raw[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) raw[k] = next[k];
+      if (r + 1 < W) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          next[k] = k < nvalid ? __ldg(reinterpret_cast<const uint4*>(p.in[r + 1]) + blk * 4 + k)
+                               : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if constexpr (!FmtInfo<F>::quant) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (k < nvalid) reinterpret_cast<uint4*>(slot + local * 64)[k] = raw[k];
+      } else {
+        bool fast;
+        const BlockScale b = raw_block_scale<F, D>(raw, nvalid, fast);
+        float x[32];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) widen8<D>(raw[k], &x[8 * k]);
+        encode_store_block<F>(x, b, fast, nvalid, slot,
+                              reinterpret_cast<uint16_t*>(slot + slot_scales_off<F>(p.chunk_nb)),
+                              reinterpret_cast<uint16_t*>(slot + slot_zps_off<F>(p.chunk_nb)), local);
       }
     }
   }
 }
 
-// Kernel 2: one thread per 8-element chunk of the message; the owner of its
-// block reduces the W source slots and requantizes into the payload.
-template <int F, int D>
-__global__ void __launch_bounds__(kDirectThreads) qr_owner_reduce_kernel(const __grid_constant__ StagedParams p) {
-  const int lane = threadIdx.x & 31;
-  const unsigned long long total = p.nb * 4;
-  const unsigned long long nchunks = p.n / 8;
-  const unsigned long long stride = (unsigned long long)gridDim.x * kDirectThreads;
-  for (unsigned long long base = (unsigned long long)blockIdx.x * kDirectThreads + (threadIdx.x & ~31u);
-       base < total; base += stride) {
-    const unsigned long long g = base + lane;
-    const bool in_block = g < total;
-    const bool valid = g < nchunks;
-    const unsigned long long blk = in_block ? (g >> 2) : 0;
-    const int c = static_cast<int>(g & 3);
-    const unsigned long long j = blk / p.chunk_nb;
-    const unsigned long long local = blk - j * p.chunk_nb;
+// Code words of chunk k of a block whose code bytes are in cw (up to 32 bytes
+// as eight 32-bit words).
+template <int F>
+__device__ __forceinline__ uint2 chunk_code_words(const uint32_t (&cw)[8], int k) {
+  if (FmtInfo<F>::bits == 8) return make_uint2(cw[2 * k], cw[2 * k + 1]);
+  if (FmtInfo<F>::bits == 4) return make_uint2(cw[k], 0u);
+  // 6 bits: chunk k's 48 bits start at bit 48k of the block's stream
+  const int bit = 48 * k, w0 = bit >> 5, sh = bit & 31;
+  const uint32_t lo = __funnelshift_r(cw[w0], cw[w0 + 1], sh);
+  const uint32_t hi = __funnelshift_r(cw[w0 + 1], w0 + 2 < 8 ? cw[w0 + 2] : 0u, sh) & 0xFFFFu;
+  return make_uint2(lo, hi);
+}
 
-    float acc[8];
+// A block's code words (up to 32 bytes), scale and zero-point from a slot.
+template <int F>
+__device__ __forceinline__ void load_slot_block(const uint8_t* slot, unsigned long long chunk_nb,
+                                                unsigned long long local, uint32_t (&cw)[8], uint16_t& s_bits,
+                                                uint16_t& z_bits) {
+  const uint8_t* cp = slot + local * FmtInfo<F>::code_bytes;
+  if (FmtInfo<F>::bits == 8) {
+    const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(cp)), a1 = __ldg(reinterpret_cast<const uint4*>(cp) + 1);
+    cw[0] = a0.x; cw[1] = a0.y; cw[2] = a0.z; cw[3] = a0.w;
+    cw[4] = a1.x; cw[5] = a1.y; cw[6] = a1.z; cw[7] = a1.w;
+  } else if (FmtInfo<F>::bits == 4) {
+    const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(cp));
+    cw[0] = a0.x; cw[1] = a0.y; cw[2] = a0.z; cw[3] = a0.w;
+    cw[4] = cw[5] = cw[6] = cw[7] = 0u;
+  } else {  // 24 bytes at an 8-byte aligned offset
+    const uint2* c2 = reinterpret_cast<const uint2*>(cp);
+    const uint2 a0 = __ldg(c2), a1 = __ldg(c2 + 1), a2 = __ldg(c2 + 2);
+    cw[0] = a0.x; cw[1] = a0.y; cw[2] = a1.x; cw[3] = a1.y; cw[4] = a2.x; cw[5] = a2.y;
+    cw[6] = cw[7] = 0u;
+  }
+  s_bits = __ldg(reinterpret_cast<const unsigned short*>(slot + slot_scales_off<F>(chunk_nb)) + local);
+  z_bits = FmtInfo<F>::asym ? __ldg(reinterpret_cast<const unsigned short*>(slot + slot_zps_off<F>(chunk_nb)) + local)
+                            : static_cast<uint16_t>(0);
+}
+
+// Kernel 2: one thread per block; the owner decodes the block from its W
+// source slots, sums them in rank order and requantizes into the payload.
+template <int F, int D>
+__global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const __grid_constant__ StagedParams p) {
+  const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
+  const int W = p.W;
+  for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
+       blk += stride) {
+    const unsigned long long rem = p.n - blk * 32;
+    const int nvalid = rem >= 32 ? 4 : static_cast<int>(rem / 8);
+    const unsigned long long j = owner_of(blk, p.chunk_nb, W);
+    const unsigned long long local = blk - j * p.chunk_nb;
+    float acc[32];
+    if constexpr (!FmtInfo<F>::quant) {
+      for (int r = 0; r < W; ++r) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.stage1 + (j * W + r) * p.slot_bytes + local * 64);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      if (r >= p.W) break;
-      const uint8_t* slot = p.stage1 + (j * p.W + r) * p.slot_bytes;
-      float y[8];
-      if constexpr (!FmtInfo<F>::quant) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) v = reinterpret_cast<const uint4*>(slot + local * 64)[c];
-        widen8<D>(v, y);
-      } else {
-        BlockScale b;
-        b.s = 0.0f;
-        b.z = 0.0f;
-        if (in_block) {
-          b.s = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(slot + slot_scales_off<F>(p.chunk_nb))[local]));
-          if (FmtInfo<F>::asym)
-            b.z = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(slot + slot_zps_off<F>(p.chunk_nb))[local]));
-          unpack8<F>(slot + local * FmtInfo<F>::code_bytes, c, b, y);
-        } else {
+        for (int k = 0; k < 4; ++k) {
+          float y[8];
+          widen8<D>(k < nvalid ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u), y);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) y[i] = 0.0f;
+          for (int i = 0; i < 8; ++i) acc[8 * k + i] = (r == 0) ? y[i] : __fadd_rn(acc[8 * k + i], y[i]);
         }
       }
-      // decoded values are exact, so this add equals the fused kernel's FMA
+      uint4* dst = reinterpret_cast<uint4*>(p.fp_values) + blk * 4;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = (r == 0) ? y[i] : __fadd_rn(acc[i], y[i]);
-    }
-
-    if constexpr (!FmtInfo<F>::quant) {
-      if (valid) reinterpret_cast<uint4*>(p.fp_values)[g] = narrow8<D>(acc);
+      for (int k = 0; k < 4; ++k)
+        if (k < nvalid) dst[k] = narrow8<D>(&acc[8 * k]);
     } else {
-      bool fast;
-      const BlockScale b2 = group_scale_f32<F>(acc, valid, fast);
-      float dec[8];
-      uint32_t packed[2] = {0u, 0u};
-      if (fast)
-        encode8<F, true>(acc, b2, dec, packed);
-      else
-        encode8<F, false>(acc, b2, dec, packed);
-      if (!valid) packed[0] = packed[1] = 0u;
-      if (in_block) store_chunk_codes<F>(p.codes, blk, c, packed);
-      if (in_block && c == 0) {
-        p.scales[blk] = b2.s_bits;
-        if (FmtInfo<F>::asym) p.zps[blk] = b2.z_bits;
+      uint32_t cw[8], ncw[8];  // this rank's and the next rank's code words
+      uint16_t sb = 0, zb = 0, nsb = 0, nzb = 0;
+      load_slot_block<F>(p.stage1 + j * W * p.slot_bytes, p.chunk_nb, local, ncw, nsb, nzb);
+      for (int r = 0; r < W; ++r) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cw[i] = ncw[i];
+        sb = nsb;
+        zb = nzb;
+        if (r + 1 < W) load_slot_block<F>(p.stage1 + (j * W + r + 1) * p.slot_bytes, p.chunk_nb, local, ncw, nsb, nzb);
+        BlockScale b;
+        b.s = __half2float(__ushort_as_half(sb));
+        b.z = FmtInfo<F>::asym ? __half2float(__ushort_as_half(zb)) : 0.0f;
+        // same bits as the fused kernel: exact products, rank order
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (r == 0)
+            unpack8_accumulate<F, true>(chunk_code_words<F>(cw, k), b, &acc[8 * k]);
+          else
+            unpack8_accumulate<F, false>(chunk_code_words<F>(cw, k), b, &acc[8 * k]);
+        }
       }
+      if (nvalid < 4 && !FmtInfo<F>::asym) {  // the symmetric statistic skips invalid chunks as zeros
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (k >= nvalid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[8 * k + i] = 0.0f;
+          }
+      }
+      bool fast;
+      const BlockScale b2 = f32_block_scale<F>(acc, nvalid, fast);
+      encode_store_block<F>(acc, b2, fast, nvalid, p.codes, p.scales, p.zps, blk);
     }
   }
 }
