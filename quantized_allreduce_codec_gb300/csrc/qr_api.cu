@@ -198,6 +198,7 @@ qr_status qr_quantize(qr_dtype dt, qr_format fmt, const void* in, size_t n, void
 
   PipeParams p;
   std::memset(&p, 0, sizeof p);
+  p.one = 1.0f;
   p.in[0] = in;
   p.W = 1;
   p.n = n;
@@ -261,6 +262,7 @@ qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages, c
 
   PipeParams p;
   std::memset(&p, 0, sizeof p);
+  p.one = 1.0f;
   for (int r = 0; r < W; ++r) p.in[r] = inputs[r];
   p.W = W;
   p.n = n;
@@ -307,6 +309,7 @@ qr_status qr_allreduce_staged(int W, qr_dtype dt, qr_format fmt, const void* con
 
   StagedParams p;
   std::memset(&p, 0, sizeof p);
+  p.one = 1.0f;
   for (int r = 0; r < W; ++r) p.in[r] = inputs[r];
   p.W = W;
   p.n = n;

@@ -107,6 +107,7 @@ extern "C" qr_status qr_allreduce_staged_noalloc(int W, qr_dtype dt, qr_format f
                              (is_asym_fmt(f) ? 2 : 0);
   StagedParams p;
   std::memset(&p, 0, sizeof p);
+  p.one = 1.0f;
   for (int r = 0; r < W; ++r) p.in[r] = inputs[r];
   p.W = W;
   p.n = n;

@@ -35,6 +35,7 @@ struct StagedParams {
   uint16_t* scales;
   uint16_t* zps;
   uint16_t* fp_values;            // FP format: payload values
+  float one;                      // 1.0f; see biased_code2
 };
 
 // Byte offsets of the regions of one slot.
@@ -97,7 +98,7 @@ __device__ __forceinline__ BlockScale f32_block_scale(const float (&x)[32], int 
 // aligned stores (32 B: two 16-byte stores; 16 B: one; Q6's 24 B: three
 // 8-byte stores).
 template <int F>
-__device__ __forceinline__ void encode_store_block(const float (&x)[32], const BlockScale& b, bool fast, int nvalid,
+__device__ __forceinline__ void encode_store_block(const float (&x)[32], const BlockScale& b, float one, bool fast, int nvalid,
                                                    uint8_t* codes, uint16_t* scales, uint16_t* zps,
                                                    unsigned long long blk) {
   uint32_t pk[4][2];
@@ -106,9 +107,9 @@ __device__ __forceinline__ void encode_store_block(const float (&x)[32], const B
     float dec[8];
     pk[k][0] = pk[k][1] = 0u;
     if (fast)
-      encode8<F, true>(&x[8 * k], b, dec, pk[k]);
+      encode8<F, true>(&x[8 * k], b, one, dec, pk[k]);
     else
-      encode8<F, false>(&x[8 * k], b, dec, pk[k]);
+      encode8<F, false>(&x[8 * k], b, one, dec, pk[k]);
     if (FmtInfo<F>::asym && k >= nvalid) pk[k][0] = pk[k][1] = 0u;  // pad codes are 0
   }
   uint8_t* cp = codes + blk * FmtInfo<F>::code_bytes;
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kStagedThreads) qr_scatter_encode_kernel(const
         float x[32];
 #pragma unroll
         for (int k = 0; k < 4; ++k) widen8<D>(raw[k], &x[8 * k]);
-        encode_store_block<F>(x, b, fast, nvalid, slot,
+        encode_store_block<F>(x, b, p.one, fast, nvalid, slot,
                               reinterpret_cast<uint16_t*>(slot + slot_scales_off<F>(p.chunk_nb)),
                               reinterpret_cast<uint16_t*>(slot + slot_zps_off<F>(p.chunk_nb)), local);
       }
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const _
       }
       bool fast;
       const BlockScale b2 = f32_block_scale<F>(acc, nvalid, fast);
-      encode_store_block<F>(acc, b2, fast, nvalid, p.codes, p.scales, p.zps, blk);
+      encode_store_block<F>(acc, b2, p.one, fast, nvalid, p.codes, p.scales, p.zps, blk);
     }
   }
 }
