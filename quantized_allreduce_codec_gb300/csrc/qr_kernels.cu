@@ -26,19 +26,19 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   auto kern = qr_pipeline_kernel<F, D, M>;
   if (ctas_per_sm[dev] == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesOf<M>);
     if (e != cudaSuccess) return e;
     int sms = 0, occ = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kSmemBytesOf<M>);
     if (e != cudaSuccess) return e;
     sm_count[dev] = sms;
     ctas_per_sm[dev] = occ > 0 ? occ : 1;
   }
   const unsigned long long max_grid = (unsigned long long)sm_count[dev] * ctas_per_sm[dev];
   const unsigned grid = static_cast<unsigned>(p.ntiles < max_grid ? p.ntiles : max_grid);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(p);
+  kern<<<grid, kThreads, kSmemBytesOf<M>, s>>>(p);
   return cudaGetLastError();
 }
 
