@@ -15,6 +15,25 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Launch with programmatic stream serialization: the kernel may become
+// resident while the previous kernel in the stream drains; it waits for that
+// kernel's completion itself (wait_prior_grid) before touching memory.
+template <typename Params>
+cudaError_t launch_overlapped(void (*kern)(Params), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                              const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <int F, int D, int M>
 cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   // Per-device launch geometry, computed once (benign race: same values).
@@ -38,8 +57,7 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   }
   const unsigned long long max_grid = (unsigned long long)sm_count[dev] * ctas_per_sm[dev];
   const unsigned grid = static_cast<unsigned>(p.ntiles < max_grid ? p.ntiles : max_grid);
-  kern<<<grid, kThreads, kSmemBytesOf<M>, s>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(kern, grid, kThreads, kSmemBytesOf<M>, s, p);
 }
 
 template <int F, int D, int M>
@@ -58,8 +76,7 @@ cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
   const unsigned long long want = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;
   const unsigned long long cap = (unsigned long long)sm_count[dev] * 16;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  qr_direct_kernel<F, D, M><<<grid, kDirectThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(qr_direct_kernel<F, D, M>, grid, kDirectThreads, 0, s, p);
 }
 
 template <int F, int D>
@@ -79,8 +96,7 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
   const unsigned long long want = (p.n / 8 + per_cta - 1) / per_cta;
   const unsigned long long cap = (unsigned long long)sm_count[dev] * 8;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  qr_decode_kernel<F, D><<<grid, kDecodeThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(qr_decode_kernel<F, D>, grid, kDecodeThreads, 0, s, p);
 }
 
 template <int F, int D>
@@ -99,11 +115,9 @@ cudaError_t launch_stg(const StagedParams& p, const DecodeParams& dp, cudaStream
   const unsigned long long cap = (unsigned long long)sm_count[dev] * 8;
   const unsigned long long want = (p.nb + kStagedThreads - 1) / kStagedThreads;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  qr_scatter_encode_kernel<F, D><<<grid, kStagedThreads, 0, s>>>(p);
-  e = cudaGetLastError();
+  e = launch_overlapped(qr_scatter_encode_kernel<F, D>, grid, kStagedThreads, 0, s, p);
   if (e != cudaSuccess) return e;
-  qr_owner_reduce_kernel<F, D><<<grid, kStagedThreads, 0, s>>>(p);
-  e = cudaGetLastError();
+  e = launch_overlapped(qr_owner_reduce_kernel<F, D>, grid, kStagedThreads, 0, s, p);
   if (e != cudaSuccess) return e;
   return launch_dec<F, D>(dp, s);
 }

@@ -135,6 +135,8 @@ __device__ __forceinline__ void encode_store_block(const float (&x)[32], const B
 // the block and write it into slot (owner, rank).
 template <int F, int D>
 __global__ void __launch_bounds__(kStagedThreads) qr_scatter_encode_kernel(const __grid_constant__ StagedParams p) {
+  wait_prior_grid();
+  allow_next_grid();
   const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
   const int W = p.W;
   for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
@@ -218,6 +220,8 @@ __device__ __forceinline__ void load_slot_block(const uint8_t* slot, unsigned lo
 // source slots, sums them in rank order and requantizes into the payload.
 template <int F, int D>
 __global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const __grid_constant__ StagedParams p) {
+  wait_prior_grid();
+  allow_next_grid();
   const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
   const int W = p.W;
   for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
