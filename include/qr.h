@@ -46,7 +46,8 @@
  *
  * Conventions for every call:
  *   - All buffers are caller-owned DEVICE memory on the current device, and
- *     must be 16-byte aligned.  The library allocates nothing.
+ *     must be 16-byte aligned (qr_allreduce_host alone takes host buffers).
+ *     The library allocates no memory.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  QR_OK means the launch was accepted; a failed launch
  *     returns QR_ERR_CUDA.  Nothing synchronises the device.
@@ -199,6 +200,53 @@ qr_status qr_allreduce_staged(int W, qr_dtype dt, qr_format fmt,
 qr_status qr_allreduce_staged_noalloc(int W, qr_dtype dt, qr_format fmt,
                                       const void *const *inputs, size_t n,
                                       void *out, void *wire, void *stream);
+
+/* Bytes of device workspace that qr_allreduce_host needs for W ranks, format
+ * fmt and chunks of chunk_elems elements: two chunk buffers, each holding W
+ * input chunks, the output chunk and the chunk's stage-2 payload, every
+ * region padded to 256 bytes.  0 for an invalid W or fmt, or a chunk_elems
+ * that is 0 or not a multiple of 32.  Host only, no CUDA call. */
+size_t qr_host_workspace_bytes(int W, qr_format fmt, size_t chunk_elems);
+
+/* qr_allreduce_emulated on HOST buffers (the quick_all_reduce call of the
+ * vLLM quick_all_reduce page with its tensors in host memory): the W input
+ * messages are read from host memory and the output (and optional stage-2
+ * payload) written to host memory.  No counterpart on the pages, which work
+ * on device tensors only; results are bit-identical to qr_allreduce_emulated
+ * on device copies of the same inputs, because the method is defined block
+ * by block.
+ *
+ * The message is processed in chunks of chunk_elems elements (a multiple of
+ * 32; the last chunk may be shorter), double-buffered in `workspace`: the
+ * copy-in of chunk i+1, the kernel on chunk i and the copy-out of chunk i-1
+ * run at the same time on the two copy directions and the SMs.
+ *   host_inputs  host array of W host pointers, n values of dtype dt each,
+ *                read only; any alignment
+ *   host_out     host, n values of dtype dt, written
+ *   host_wire    host, qr_encoded_bytes(fmt, n) bytes in the layout of
+ *                qr_allreduce_emulated's wire, written; or NULL.  Must be NULL
+ *                when stages == 1
+ *   workspace    device, at least qr_host_workspace_bytes(W, fmt,
+ *                chunk_elems) bytes (workspace_bytes says how many), 16-byte
+ *                aligned, owned by the caller; no other work may use it until
+ *                this call's work on `stream` has completed
+ * Host buffers should be page-locked (cudaHostAlloc or cudaHostRegister):
+ * copies from or to pageable memory are correct but do not overlap.
+ * Ordering: everything is ordered after prior work on `stream`, and work
+ * later enqueued on `stream` runs after all of it, the last copy-out
+ * included; the host buffers may be read or reused from then on.  The copies
+ * run on two streams that the library creates per device on first use and
+ * keeps; calls on one device enqueue one at a time (a mutex).  Not meant
+ * for CUDA graph capture (use qr_allreduce_emulated inside graphs).
+ * Errors: as qr_allreduce_emulated, plus QR_ERR_SIZE for a bad chunk_elems
+ * or too small a workspace, QR_ERR_OVERLAP for host buffers that overlap;
+ * QR_ERR_CUDA if a copy or a launch is refused (work enqueued before the
+ * failure still runs). */
+qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages,
+                            const void *const *host_inputs, size_t n,
+                            void *host_out, void *host_wire, void *workspace,
+                            size_t workspace_bytes, size_t chunk_elems,
+                            void *stream);
 
 /* Messages of at most qr_direct_limit() elements per rank are processed by a
  * single-pass kernel with one memory round trip (lowest latency); longer ones

@@ -27,7 +27,8 @@ LIB_PATH = os.path.join(_HERE, "libqr.so")
 EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
            "qr_status_string", "qr_device_error", "qr_direct_limit", "qr_set_direct_limit",
            "qr_selftest_wait_timeout", "qr_stage1_bytes", "qr_allreduce_staged",
-           "qr_allreduce_staged_noalloc")
+           "qr_allreduce_staged_noalloc", "qr_host_workspace_bytes", "qr_allreduce_host")
+DEFAULT_HOST_CHUNK = 1 << 22  # elements per rank per chunk of qr_allreduce_host (8 MiB of fp16)
 
 _lib = None
 _lock = threading.Lock()
@@ -75,6 +76,10 @@ def lib():
                 L.qr_allreduce_staged.argtypes = [i, i, i, vp, sz, vp, vp, vp, vp]
                 L.qr_allreduce_staged_noalloc.restype = i
                 L.qr_allreduce_staged_noalloc.argtypes = [i, i, i, vp, sz, vp, vp, vp]
+                L.qr_host_workspace_bytes.restype = sz
+                L.qr_host_workspace_bytes.argtypes = [i, i, sz]
+                L.qr_allreduce_host.restype = i
+                L.qr_allreduce_host.argtypes = [i, i, i, i, vp, sz, vp, vp, vp, sz, sz, vp]
                 L.qr_selftest_wait_timeout.restype = i
                 L.qr_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
                 _lib = L
@@ -86,6 +91,10 @@ def _addr(x) -> int | None:
         return None
     if isinstance(x, int):
         return x
+    if hasattr(x, "__array_interface__"):  # numpy array (host memory)
+        if not x.flags["C_CONTIGUOUS"]:
+            raise ValueError("arrays must be C-contiguous")
+        return x.ctypes.data
     if not x.is_contiguous():
         raise ValueError("tensors must be contiguous")
     return x.data_ptr()
@@ -200,3 +209,38 @@ def qr_allreduce_staged_noalloc(W: int, dtype, fmt: int, inputs, n: int, out, wi
                                              ctypes.cast(ptrs, ctypes.c_void_p) if inputs else None, n,
                                              _addr(out), _addr(wire), _stream(stream)),
            "qr_allreduce_staged_noalloc")
+
+
+def qr_host_workspace_bytes(W: int, fmt: int, chunk_elems: int = DEFAULT_HOST_CHUNK) -> int:
+    """Device workspace bytes qr_allreduce_host needs (0: invalid arguments)."""
+    return int(lib().qr_host_workspace_bytes(W, fmt, chunk_elems))
+
+
+def host_workspace(W: int, fmt: int, chunk_elems: int = DEFAULT_HOST_CHUNK, device=None):
+    """A device byte tensor large enough to serve as qr_allreduce_host's
+    workspace (memory from torch's allocator)."""
+    import torch
+    nbytes = qr_host_workspace_bytes(W, fmt, chunk_elems)
+    if nbytes == 0:
+        raise ValueError("invalid W, format or chunk size")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def qr_allreduce_host(W: int, dtype, fmt: int, stages: int, host_inputs, n: int, host_out,
+                      host_wire=None, workspace=None, workspace_bytes: int | None = None,
+                      chunk_elems: int = DEFAULT_HOST_CHUNK, stream=None) -> None:
+    """qr_allreduce_emulated on host buffers (CPU tensors or numpy arrays,
+    page-locked for overlapped copies), chunked through a device workspace
+    (see host_workspace); the copies and the kernels overlap."""
+    if workspace is None:
+        raise ValueError("qr_allreduce_host needs a device workspace (see host_workspace)")
+    if workspace_bytes is None:
+        if isinstance(workspace, int):
+            raise ValueError("workspace_bytes is required with a raw workspace address")
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    ptrs = (ctypes.c_void_p * max(len(host_inputs), 1))(*[_addr(x) for x in host_inputs])
+    _check(lib().qr_allreduce_host(W, _dtype_code(dtype), fmt, stages,
+                                   ctypes.cast(ptrs, ctypes.c_void_p) if host_inputs else None, n,
+                                   _addr(host_out), _addr(host_wire), _addr(workspace), workspace_bytes,
+                                   chunk_elems, _stream(stream)),
+           "qr_allreduce_host")

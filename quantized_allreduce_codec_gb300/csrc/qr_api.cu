@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "qr.h"
 #include "qr_launch.h"
@@ -137,6 +138,50 @@ __global__ void qr_selftest_wait_kernel(unsigned* err, unsigned long long limit_
   __syncthreads();
   const bool completed = mbar_wait(&bar, 0u, limit_ns);
   if (!__all_sync(0xffffffffu, completed) && threadIdx.x == 0) atomicOr(err, kErrSelfTest);
+}
+
+// ---- qr_allreduce_host: per-device copy streams and reusable events ----
+// Chunk i uses buffer i & 1.  in_done[b]: its copy-in finished; k_done[b]:
+// its kernel finished (the inputs may be overwritten); out_done[b]: its
+// copy-out finished (the output may be overwritten).
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t in_done[2] = {nullptr, nullptr}, k_done[2] = {nullptr, nullptr}, out_done[2] = {nullptr, nullptr};
+};
+HostPipe g_host_pipe[kMaxDevices];
+std::mutex g_host_mutex[kMaxDevices];
+
+cudaError_t host_pipe_ready(HostPipe& h) {
+  if (h.ready) return cudaSuccess;
+  cudaError_t e = cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
+  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+    e = cudaEventCreateWithFlags(&h.in_done[b], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.k_done[b], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.out_done[b], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) {  // release what was made; the next call tries again
+    if (h.s_in) cudaStreamDestroy(h.s_in);
+    if (h.s_out) cudaStreamDestroy(h.s_out);
+    cudaEvent_t* evs[] = {&h.start, &h.in_done[0], &h.in_done[1], &h.k_done[0], &h.k_done[1], &h.out_done[0],
+                          &h.out_done[1]};
+    for (cudaEvent_t* ev : evs)
+      if (*ev) cudaEventDestroy(*ev);
+    h = HostPipe();
+    return e;
+  }
+  h.ready = true;
+  return cudaSuccess;
+}
+
+size_t pad256(size_t bytes) { return (bytes + 255) / 256 * 256; }
+
+// One chunk buffer of the host-entry workspace: W inputs | output | payload.
+size_t host_chunk_buffer_bytes(int W, int fmt, size_t chunk) {
+  return static_cast<size_t>(W + 1) * pad256(chunk * 2) + pad256(qr_encoded_bytes(static_cast<qr_format>(fmt), chunk));
 }
 
 }  // namespace
@@ -333,6 +378,120 @@ qr_status qr_allreduce_staged(int W, qr_dtype dt, qr_format fmt, const void* con
   dp.err = device_error_word();
   if (!dp.err) return QR_ERR_CUDA;
   return to_status(dispatch_staged(f, d, p, dp, static_cast<cudaStream_t>(stream)));
+}
+
+size_t qr_host_workspace_bytes(int W, qr_format fmt, size_t chunk_elems) {
+  const int f = static_cast<int>(fmt);
+  if ((W != 1 && W != 2 && W != 4 && W != 8) || !valid_format(f)) return 0;
+  if (chunk_elems == 0 || chunk_elems % 32 != 0 || chunk_elems > QR_MAX_ELEMS) return 0;
+  return 2 * host_chunk_buffer_bytes(W, f, chunk_elems);
+}
+
+qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages, const void* const* host_inputs,
+                            size_t n, void* host_out, void* host_wire, void* workspace, size_t workspace_bytes,
+                            size_t chunk_elems, void* stream) {
+  const int f = static_cast<int>(fmt), d = static_cast<int>(dt);
+  if (n && (!host_inputs || !host_out || !workspace)) return QR_ERR_NULL;
+  if (!valid_dtype(d) && d != DT_BF16_AS_F16) return QR_ERR_DTYPE;
+  if (!valid_format(f)) return QR_ERR_FORMAT;
+  if (W != 1 && W != 2 && W != 4 && W != 8) return QR_ERR_WORLD;
+  if (stages != 1 && stages != 2) return QR_ERR_STAGES;
+  if (stages == 1 && host_wire) return QR_ERR_STAGES;
+  qr_status st = check_size(n);
+  if (st != QR_OK) return st;
+  const size_t need = qr_host_workspace_bytes(W, fmt, chunk_elems);
+  if (need == 0 || workspace_bytes < need) return QR_ERR_SIZE;
+  if (n == 0) return QR_OK;
+  for (int r = 0; r < W; ++r)
+    if (!host_inputs[r]) return QR_ERR_NULL;
+  if (!aligned16(workspace)) return QR_ERR_ALIGN;
+  const size_t msg = n * 2, wbytes = host_wire ? qr_encoded_bytes(fmt, n) : 0;
+  for (int r = 0; r < W; ++r)
+    if (overlap(host_inputs[r], msg, host_out, msg) || overlap(host_inputs[r], msg, host_wire, wbytes))
+      return QR_ERR_OVERLAP;
+  if (overlap(host_out, msg, host_wire, wbytes)) return QR_ERR_OVERLAP;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QR_ERR_CUDA;
+  unsigned* err = device_error_word();
+  if (!err) return QR_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_host_mutex[dev]);
+  HostPipe& h = g_host_pipe[dev];
+  if (host_pipe_ready(h) != cudaSuccess) return QR_ERR_CUDA;
+
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t nb = (n + 31) / 32;
+  const size_t cb = 32 * static_cast<size_t>(code_bits(f)) / 8;
+  const size_t buf_bytes = host_chunk_buffer_bytes(W, f, chunk_elems);
+  const size_t nchunks = (n + chunk_elems - 1) / chunk_elems;
+  const int mode = stages == 1 ? MODE_AR1 : MODE_AR2;
+  uint8_t* hwire = static_cast<uint8_t*>(host_wire);
+  uint8_t* hout = static_cast<uint8_t*>(host_out);
+
+#define QR_TRY(call)                               \
+  do {                                             \
+    if ((call) != cudaSuccess) return QR_ERR_CUDA; \
+  } while (0)
+  // both copy streams start after the work already on `stream`
+  QR_TRY(cudaEventRecord(h.start, s));
+  QR_TRY(cudaStreamWaitEvent(h.s_in, h.start, 0));
+  QR_TRY(cudaStreamWaitEvent(h.s_out, h.start, 0));
+  for (size_t i = 0; i < nchunks; ++i) {
+    const int b = static_cast<int>(i & 1);
+    uint8_t* base = static_cast<uint8_t*>(workspace) + b * buf_bytes;
+    uint8_t* d_out = base + static_cast<size_t>(W) * pad256(chunk_elems * 2);
+    uint8_t* d_wire = d_out + pad256(chunk_elems * 2);
+    const size_t c0 = i * chunk_elems;
+    const size_t cn = (n - c0) < chunk_elems ? (n - c0) : chunk_elems;
+    const size_t blk0 = c0 / 32, nbc = (cn + 31) / 32;
+
+    // copy-in: buffer b is free once chunk i-2's kernel has read it
+    if (i >= 2) QR_TRY(cudaStreamWaitEvent(h.s_in, h.k_done[b], 0));
+    for (int r = 0; r < W; ++r)
+      QR_TRY(cudaMemcpyAsync(base + r * pad256(chunk_elems * 2), static_cast<const uint8_t*>(host_inputs[r]) + c0 * 2,
+                             cn * 2, cudaMemcpyHostToDevice, h.s_in));
+    QR_TRY(cudaEventRecord(h.in_done[b], h.s_in));
+
+    // kernel on the caller's stream: after the copy-in, and after chunk i-2's
+    // copy-out has read this buffer's output and payload
+    QR_TRY(cudaStreamWaitEvent(s, h.in_done[b], 0));
+    if (i >= 2) QR_TRY(cudaStreamWaitEvent(s, h.out_done[b], 0));
+    PipeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.one = 1.0f;
+    for (int r = 0; r < W; ++r) p.in[r] = base + r * pad256(chunk_elems * 2);
+    p.W = W;
+    p.n = cn;
+    p.nb = nbc;
+    p.ntiles = (cn + kTileElems - 1) / kTileElems;
+    p.out = d_out;
+    if (stages == 2 && host_wire) encoded_regions(f, cn, d_wire, &p.codes, &p.scales, &p.zps, &p.fp_values);
+    p.err = err;
+    QR_TRY(dispatch_pipeline(f, d, mode, p, s));
+    QR_TRY(cudaEventRecord(h.k_done[b], s));
+
+    // copy-out into the message-wide host layout
+    QR_TRY(cudaStreamWaitEvent(h.s_out, h.k_done[b], 0));
+    QR_TRY(cudaMemcpyAsync(hout + c0 * 2, d_out, cn * 2, cudaMemcpyDeviceToHost, h.s_out));
+    if (hwire) {
+      if (f == FMT_FP) {
+        QR_TRY(cudaMemcpyAsync(hwire + c0 * 2, d_wire, cn * 2, cudaMemcpyDeviceToHost, h.s_out));
+      } else {
+        QR_TRY(cudaMemcpyAsync(hwire + blk0 * cb, d_wire, nbc * cb, cudaMemcpyDeviceToHost, h.s_out));
+        QR_TRY(cudaMemcpyAsync(hwire + nb * cb + blk0 * 2, d_wire + nbc * cb, nbc * 2, cudaMemcpyDeviceToHost,
+                               h.s_out));
+        if (is_asym(f))
+          QR_TRY(cudaMemcpyAsync(hwire + nb * cb + nb * 2 + blk0 * 2, d_wire + nbc * cb + nbc * 2, nbc * 2,
+                                 cudaMemcpyDeviceToHost, h.s_out));
+      }
+    }
+    QR_TRY(cudaEventRecord(h.out_done[b], h.s_out));
+  }
+  // the caller's stream continues after the last copy-out (the copy-out
+  // stream runs in order, so that covers every chunk)
+  QR_TRY(cudaStreamWaitEvent(s, h.out_done[(nchunks - 1) & 1], 0));
+#undef QR_TRY
+  return QR_OK;
 }
 
 size_t qr_direct_limit(void) { return static_cast<size_t>(g_direct_limit.load()); }

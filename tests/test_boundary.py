@@ -159,3 +159,46 @@ def test_stage1_bytes_geometry(L):
                 assert qr.qr_stage1_bytes(W, fmt, n) == W * W * ((cnb * per_block + 15) // 16 * 16)
     assert qr.qr_stage1_bytes(3, 1, 64) == 0
     assert qr.qr_stage1_bytes(2, 9, 64) == 0
+
+
+def test_host_workspace_bytes_geometry(L):
+    # two chunk buffers of W inputs + output + payload, each region padded to 256 bytes
+    pad = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    for W in (1, 2, 4, 8):
+        for fmt in range(7):
+            for chunk in (32, 8192, 1 << 21, (1 << 21) + 96):
+                want = 2 * ((W + 1) * pad(chunk * 2) + pad(qr.qr_encoded_bytes(fmt, chunk)))
+                assert qr.qr_host_workspace_bytes(W, fmt, chunk) == want
+    assert qr.qr_host_workspace_bytes(2, 1, 0) == 0       # chunk of 0
+    assert qr.qr_host_workspace_bytes(2, 1, 48) == 0      # not whole blocks
+    assert qr.qr_host_workspace_bytes(3, 1, 64) == 0      # W
+    assert qr.qr_host_workspace_bytes(2, 7, 64) == 0      # format
+
+
+def _host(W, dt, fmt, stages, inputs, n, out, wire, ws, ws_bytes, chunk):
+    arr = (ctypes.c_void_p * max(len(inputs), 1))(*inputs)
+    return qr.lib().qr_allreduce_host(W, dt, fmt, stages, ctypes.cast(arr, ctypes.c_void_p), n, out, wire,
+                                      ws, ws_bytes, chunk, None)
+
+
+def test_host_entry_argument_errors(L):
+    # host buffers need no alignment; every check runs before any CUDA call
+    ha, hb, hc = 0x10000001, 0x20000003, 0x30000005
+    chunk = 1 << 12
+    need = qr.qr_host_workspace_bytes(2, 1, chunk)
+    ok = dict(ws=C, ws_bytes=need, chunk=chunk)
+    assert _host(2, 0, 1, 2, [ha, hb], 0, None, None, **ok) == 0            # empty message
+    assert _host(2, 0, 1, 2, [ha, hb], 64, None, None, **ok) == 1           # QR_ERR_NULL (out)
+    assert _host(2, 0, 1, 2, [ha, 0], 64, hc, None, **ok) == 1              # NULL rank pointer
+    assert _host(2, 0, 1, 2, [ha, hb], 64, hc, None, None, need, chunk) == 1  # no workspace
+    assert _host(2, 3, 1, 2, [ha, hb], 64, hc, None, **ok) == 2             # QR_ERR_DTYPE
+    assert _host(2, 0, 9, 2, [ha, hb], 64, hc, None, **ok) == 3             # QR_ERR_FORMAT
+    assert _host(3, 0, 1, 2, [ha, hb, ha], 64, hc, None, **ok) == 4         # QR_ERR_WORLD
+    assert _host(2, 0, 1, 1, [ha, hb], 64, hc, hc + (1 << 20), **ok) == 5   # wire with one stage
+    assert _host(2, 0, 1, 2, [ha, hb], 60, hc, None, **ok) == 6             # not % 16 bytes
+    assert _host(2, 0, 1, 2, [ha, hb], 64, hc, None, C, need - 1, chunk) == 6  # workspace too small
+    assert _host(2, 0, 1, 2, [ha, hb], 64, hc, None, C, need, 40) == 6      # chunk not whole blocks
+    assert _host(2, 0, 1, 2, [ha, hb], 64, hc, None, C + 8, need, chunk) == 7  # workspace alignment
+    assert _host(2, 0, 1, 2, [ha, hb], 64, ha + 100, None, **ok) == 8       # out overlaps an input
+    assert _host(2, 0, 1, 2, [ha, hb], 64, hc, hb + 2, **ok) == 8           # wire overlaps an input
+    assert _host(2, 0, 1, 2, [ha, hb], 64, hc, hc + 64, **ok) == 8          # wire overlaps out
