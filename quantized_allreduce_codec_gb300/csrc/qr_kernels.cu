@@ -34,6 +34,29 @@ cudaError_t launch_overlapped(void (*kern)(Params), unsigned grid, unsigned bloc
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// CTAs of `kern` that are resident on the current device at once (SMs x
+// CTAs per SM at this block size and shared memory), computed once per
+// device; grid-stride kernels are launched with at most this many, so every
+// CTA starts at once and none waits for a second wave.
+template <typename Params>
+cudaError_t resident_ctas(void (*kern)(Params), int threads, int smem, unsigned long long* cache,
+                          unsigned long long* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (cache[dev] == 0) {
+    int sms = 0, occ = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    cache[dev] = static_cast<unsigned long long>(sms) * static_cast<unsigned long long>(occ > 0 ? occ : 1);
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
+
 template <int F, int D, int M>
 cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   // Per-device launch geometry, computed once (benign race: same values).
@@ -62,62 +85,41 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
 
 template <int F, int D, int M>
 cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
-  static int sm_count[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static unsigned long long cap[kMaxDevices];
+  unsigned long long max_grid = 0;
+  cudaError_t e = resident_ctas(qr_direct_kernel<F, D, M>, kDirectThreads, 0, cap, &max_grid);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (sm_count[dev] == 0) {
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sm_count[dev] = sms;
-  }
   const unsigned long long want = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;
-  const unsigned long long cap = (unsigned long long)sm_count[dev] * 16;
-  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  const unsigned grid = static_cast<unsigned>(want < max_grid ? want : max_grid);
   return launch_overlapped(qr_direct_kernel<F, D, M>, grid, kDirectThreads, 0, s, p);
 }
 
 template <int F, int D>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
-  static int sm_count[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static unsigned long long cap[kMaxDevices];
+  unsigned long long max_grid = 0;
+  cudaError_t e = resident_ctas(qr_decode_kernel<F, D>, kDecodeThreads, 0, cap, &max_grid);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (sm_count[dev] == 0) {
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sm_count[dev] = sms;
-  }
   const unsigned long long per_cta = (unsigned long long)kDecodeThreads * kDecodeUnroll;
   const unsigned long long want = (p.n / 8 + per_cta - 1) / per_cta;
-  const unsigned long long cap = (unsigned long long)sm_count[dev] * 8;
-  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  const unsigned grid = static_cast<unsigned>(want < max_grid ? want : max_grid);
   return launch_overlapped(qr_decode_kernel<F, D>, grid, kDecodeThreads, 0, s, p);
 }
 
 template <int F, int D>
 cudaError_t launch_stg(const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
-  static int sm_count[kMaxDevices];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static unsigned long long cap1[kMaxDevices], cap2[kMaxDevices];
+  unsigned long long max1 = 0, max2 = 0;
+  cudaError_t e = resident_ctas(qr_scatter_encode_kernel<F, D>, kStagedThreads, 0, cap1, &max1);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (sm_count[dev] == 0) {
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sm_count[dev] = sms;
-  }
-  const unsigned long long cap = (unsigned long long)sm_count[dev] * 8;
+  e = resident_ctas(qr_owner_reduce_kernel<F, D>, kStagedThreads, 0, cap2, &max2);
+  if (e != cudaSuccess) return e;
   const unsigned long long want = (p.nb + kStagedThreads - 1) / kStagedThreads;
-  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
-  e = launch_overlapped(qr_scatter_encode_kernel<F, D>, grid, kStagedThreads, 0, s, p);
+  e = launch_overlapped(qr_scatter_encode_kernel<F, D>, static_cast<unsigned>(want < max1 ? want : max1),
+                        kStagedThreads, 0, s, p);
   if (e != cudaSuccess) return e;
-  e = launch_overlapped(qr_owner_reduce_kernel<F, D>, grid, kStagedThreads, 0, s, p);
+  e = launch_overlapped(qr_owner_reduce_kernel<F, D>, static_cast<unsigned>(want < max2 ? want : max2),
+                        kStagedThreads, 0, s, p);
   if (e != cudaSuccess) return e;
   return launch_dec<F, D>(dp, s);
 }
