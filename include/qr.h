@@ -51,6 +51,14 @@
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  QR_OK means the launch was accepted; a failed launch
  *     returns QR_ERR_CUDA.  Nothing synchronises the device.
+ *   - Kernels are launched with programmatic stream serialization: each may
+ *     become resident while the previous kernel on the stream drains, and
+ *     waits for that kernel's completion before touching memory.  Each also
+ *     lets the next kernel be scheduled early, so a kernel the caller
+ *     launches after a call WITH that same attribute must call
+ *     cudaGridDependencySynchronize() before reading the call's outputs (the
+ *     general rule for programmatic dependent launch); ordinary launches,
+ *     copies and events see the usual stream order.
  *   - n == 0 is a valid empty message: nothing is launched and pointers may
  *     be NULL.
  *   - Errors are reported by the return value only; no call aborts or
