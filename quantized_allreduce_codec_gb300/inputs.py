@@ -123,3 +123,19 @@ def sweep_workload(size_bytes: int) -> Workload:
     """One point of the tp2 size sweep (W=2, fp16, N(0,1))."""
     return Workload(2, f"W2-fp16-{size_bytes}B", 2, F16, size_bytes // 2, "normal",
                     (FP, FP8, Q8, Q6, Q4), (1, 2))
+
+
+def long_message_bits(seed: int, n: int, dtype: int, tile: int = 1 << 20) -> np.ndarray:
+    """A message of n values too long to draw value by value in a test (for
+    checks of 64-bit offsets past 2^31 elements): one N(0, 1) tile of `tile`
+    values drawn with `seed`, repeated, tile i scaled by 2^((5*i mod 13) - 6)
+    before the rounding to dtype.  Tiles whose indices differ by a
+    power of two never share a scale (13 is prime), so a 32-bit offset that
+    wrapped would read different values."""
+    base = np.random.default_rng(seed).standard_normal(tile, dtype=np.float32)
+    variants = [to_bits(base * np.float32(2.0 ** (s - 6)), dtype) for s in range(13)]
+    out = np.empty(n, np.uint16)
+    for i, start in enumerate(range(0, n, tile)):
+        stop = min(start + tile, n)
+        out[start:stop] = variants[(5 * i) % 13][:stop - start]
+    return out
