@@ -44,7 +44,7 @@ if ROOT not in sys.path:
 
 from quantized_allreduce_codec_gb300.inputs import (BF16, F16, FORMAT_NAMES, FP, FP8, Q4,  # noqa: E402
                                                     Q4A, Q6, Q8, Q8A, from_bits, sweep_sizes_bytes,
-                                                    sweep_workload, workloads)
+                                                    sweep_workload, workloads, Workload)
 
 METRIC = "emulated quick-allreduce GB/s per rank-message and % of HBM roofline, 1×GB300"
 STEP_CALLS = [(FP, 1), (FP, 2), (FP8, 2), (Q8, 2), (Q6, 2), (Q4, 2)]  # the tp2 table's kernels
@@ -537,6 +537,8 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(host, wl.dtype, args.cpu_seconds)
+        if not args.no_extras:
+            cpu["per_config_GBps"] = oracle_per_config(cpu["cores"])
 
     if rank == 0:
         line = {
@@ -566,13 +568,14 @@ def run_ours(args):
     dist_barrier()
 
 
-def oracle_step(dtype, xs, threads: int) -> None:
-    """One bench step (the six calls) through the oracle, the message split
-    into `threads` contiguous runs of whole 32-element blocks, one per host
-    thread.  The oracle is a C library called through ctypes, which releases
-    the GIL, and the result is defined block by block, so the runs are
-    independent; the oracle itself is unchanged."""
+def oracle_step(dtype, xs, threads: int, calls=None) -> None:
+    """One bench step (the six calls, or `calls`) through the oracle, the
+    message split into `threads` contiguous runs of whole 32-element blocks,
+    one per host thread.  The oracle is a C library called through ctypes,
+    which releases the GIL, and the result is defined block by block, so the
+    runs are independent; the oracle itself is unchanged."""
     import oracle
+    calls = STEP_CALLS if calls is None else calls
     m = xs[0].size
     nblk = m // 32
     cuts = [(nblk * i // threads) * 32 for i in range(threads)] + [m]
@@ -580,7 +583,7 @@ def oracle_step(dtype, xs, threads: int) -> None:
 
     def one(lo_hi):
         lo, hi = lo_hi
-        for fmt, st in STEP_CALLS:
+        for fmt, st in calls:
             oracle.allreduce(dtype, fmt, st, [x[lo:hi] for x in xs])
 
     if len(parts) == 1:
@@ -589,6 +592,30 @@ def oracle_step(dtype, xs, threads: int) -> None:
     from concurrent.futures import ThreadPoolExecutor
     with ThreadPoolExecutor(max_workers=len(parts)) as ex:
         list(ex.map(one, parts))
+
+
+def oracle_per_config(threads: int, m: int = 1 << 20) -> dict:
+    """The oracle on each of the five workloads' recipes at a bounded size
+    (min(n, m) elements per rank, same generator, shape and value mix), per
+    format and stage count, on `threads` host threads: GB/s per
+    rank-message."""
+    import oracle
+    oracle.build()
+    res = {}
+    for w in workloads().values():
+        mm = min(w.n, m)
+        small = Workload(w.key, w.name, w.W, w.dtype, mm, w.kind, w.formats, w.stages,
+                         rows=w.rows if (w.rows and mm % w.rows == 0) else None, sigma=w.sigma)
+        xs = small.inputs()
+        row = {}
+        for fmt in w.formats:
+            for st in w.stages:
+                t0 = time.perf_counter()
+                oracle_step(w.dtype, xs, threads, [(fmt, st)])
+                t = time.perf_counter() - t0
+                row[step_name(fmt, st)] = round(mm * 2 / t / 1e9, 5)
+        res[f"{w.name} (first {mm} elements per rank)"] = row
+    return res
 
 
 def host_threads() -> int:
