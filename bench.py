@@ -78,6 +78,47 @@ def bytes_alg_staged(W: int, n: int, fmt: int) -> int:
     return (W + 1) * n * 2 + (2 * W + 2) * c
 
 
+QMAX = {Q8: 127, Q6: 31, Q4: 7}
+
+
+def error_vs_exact(host, out_bits, dtype, fmt, stages) -> dict:
+    """Deviation of an allreduce output from the fp64 exact sum e of the
+    inputs, against the stated bounds: FP within 1 ulp of the dtype; FP8
+    within 2^-3 of sum_r |x_r|; a symmetric integer format within
+    b1 = sum_r s_r/2 (stage 1, s_r = fp16(max|x_r| / Qmax) per block) plus,
+    for two stages, s2/2 with s2 <= (max|e| + b1) / Qmax * (1 + 2^-10) per
+    block, plus 1/2 ulp of the dtype and the binary32 summation error.
+    Also reported: the largest per-block ratio max|y - e| / max sum_r|x_r|."""
+    xs = [from_bits(h, dtype).astype(np.float64) for h in host]
+    e = np.sum(xs, axis=0)
+    sabs = np.sum([np.abs(x) for x in xs], axis=0)
+    y = from_bits(out_bits, dtype).astype(np.float64)
+    nb = e.size // 32
+    m = nb * 32
+    err = np.abs(y - e)[:m]
+    mant = 10 if dtype == F16 else 7
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(e[:m]), 2.0 ** -24))) - mant)
+    blk = lambda v: np.repeat(np.abs(v[:m]).reshape(nb, 32).max(axis=1), 32)  # noqa: E731
+    res = {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
+           "max_block_rel": float((blk(err) / np.maximum(blk(sabs), 1e-300)).max())}
+    if fmt == FP:
+        bound = ulp
+    elif fmt == FP8:
+        bound = 2.0 ** -3 * sabs[:m] + ulp
+    elif fmt in QMAX:
+        q = QMAX[fmt]
+        b1 = np.zeros(m)
+        for x in xs:
+            b1 += (blk(x) / q).astype(np.float16).astype(np.float64) / 2
+        bound = b1 + ulp + 2.0 ** -20 * sabs[:m]
+        if stages == 2:
+            bound += (blk(e) + blk(b1)) / q * (1 + 2.0 ** -10) / 2
+    else:
+        return res
+    res["within_bound_fraction"] = float(np.mean(err <= bound))
+    return res
+
+
 def step_name(fmt: int, stages: int) -> str:
     return f"{FORMAT_NAMES[fmt]}-{stages}stage"
 
@@ -366,6 +407,15 @@ def run_ours(args):
             q_bytes += b
             q_time += t
     achieved = q_bytes / q_time / 1e9
+
+    # ---------------- deviation from the exact sum, per format (rank 0) ----------------
+    errors = {}
+    if rank == 0 and not args.no_extras:
+        for fmt, st in STEP_CALLS:
+            call(fmt, st)
+            torch.cuda.synchronize()
+            errors[step_name(fmt, st)] = error_vs_exact(host, out.cpu().numpy().view(np.uint16), wl.dtype,
+                                                         fmt, st)
     traffic = recorded_traffic(os.path.join(ROOT, "quantized_allreduce_codec_gb300", "csrc",
                                             "qr_device.cuh"))
     roofline = {"kernel": "qr_pipeline_kernel (fused two-stage, quantized formats FP8/Q8/Q6/Q4, fp16, W=2)",
@@ -556,7 +606,7 @@ def run_ours(args):
                              f"{flush_buf.numel() * 4 >> 20} MiB write, then a {clean_buf.numel() * 4 >> 20} MiB "
                              "read of a second buffer (no dirty lines left in L2)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, W ranks emulated in HBM"},
-            "roofline": roofline, "per_format": per_format,
+            "roofline": roofline, "per_format": per_format, "error_vs_exact_sum": errors,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": K * len(STEP_CALLS),
             "clocks": clocks, "wall_ms_per_step_incl_flush": round(wall / K * 1e3, 3),
