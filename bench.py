@@ -462,13 +462,12 @@ def run_ours(args):
                    "the device)"}
     del pin_in, pin_out, workspace
 
-    # ---------------- size sweep (tp2 table sizes) ----------------
+    # ---------------- size sweep (tp2 table sizes, then 128 MiB) ----------------
     sweep = {}
     if not args.no_extras:
         default_limit = qr.qr_direct_limit()
-        for size in sweep_sizes_bytes():
-            nn = size // 2
-            sub = [t[:nn] for t in ins]
+
+        def sweep_point(nn, sub, o, wdict):
             row = {}
             # both kernels are timed at every size (the default routing picks one)
             paths = [("default", default_limit), ("direct", (1 << 64) - 1), ("pipeline", 0)]
@@ -476,7 +475,10 @@ def run_ours(args):
                 entry = {}
                 for pname, limit in paths:
                     qr.qr_set_direct_limit(limit)
-                    t = per_call_seconds(lambda: call(fmt, st, sub, nn, out), args.sweep_reps)
+                    t = per_call_seconds(
+                        lambda: qr.qr_allreduce_emulated(W, wl.dtype, fmt, st, sub, nn, o,
+                                                         wdict[fmt] if st == 2 else None, None),
+                        args.sweep_reps)
                     if pname == "default":
                         entry.update({"us": round(t * 1e6, 2),
                                       "hbm_frac": round(bytes_alg(W, nn, fmt, st, st == 2) / t / 1e9 / peak, 3)})
@@ -484,7 +486,19 @@ def run_ours(args):
                         entry[f"us_{pname}"] = round(t * 1e6, 2)
                 qr.qr_set_direct_limit(default_limit)
                 row[step_name(fmt, st)] = entry
-            sweep[str(size)] = row
+            return row
+
+        for size in sweep_sizes_bytes():
+            nn = size // 2
+            sweep[str(size)] = sweep_point(nn, [t[:nn] for t in ins], out, wires)
+        # one point past the tp2 table: 128 MiB per rank, its own buffers
+        big = sweep_workload(128 << 20)
+        big_ins = [torch.from_numpy(x.view(np.int16)).to(dev) for x in big.inputs()]
+        big_out = torch.empty(big.n, dtype=torch.int16, device=dev)
+        big_wires = {f: torch.empty(encoded_bytes(f, big.n), dtype=torch.uint8, device=dev) for f, _ in STEP_CALLS}
+        sweep[str(128 << 20)] = sweep_point(big.n, big_ins, big_out, big_wires)
+        del big_ins, big_out, big_wires
+        torch.cuda.empty_cache()
 
     # ---------------- the codec on its own (qr_quantize / qr_dequantize) ----------------
     codec = {}
