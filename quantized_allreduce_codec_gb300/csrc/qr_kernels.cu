@@ -83,15 +83,21 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   return launch_overlapped(kern, grid, kThreads, kSmemBytesOf<M>, s, p);
 }
 
-template <int F, int D, int M>
-cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
+template <int F, int D, int M, int WS>
+cudaError_t launch_dir_w(const PipeParams& p, cudaStream_t s) {
   static unsigned long long cap[kMaxDevices];
   unsigned long long max_grid = 0;
-  cudaError_t e = resident_ctas(qr_direct_kernel<F, D, M>, kDirectThreads, 0, cap, &max_grid);
+  cudaError_t e = resident_ctas(qr_direct_kernel<F, D, M, WS>, kDirectThreads, 0, cap, &max_grid);
   if (e != cudaSuccess) return e;
   const unsigned long long want = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;
   const unsigned grid = static_cast<unsigned>(want < max_grid ? want : max_grid);
-  return launch_overlapped(qr_direct_kernel<F, D, M>, grid, kDirectThreads, 0, s, p);
+  return launch_overlapped(qr_direct_kernel<F, D, M, WS>, grid, kDirectThreads, 0, s, p);
+}
+
+// W = 2 (the tp2 case) has its own instantiation with the rank count known.
+template <int F, int D, int M>
+cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
+  return p.W == 2 ? launch_dir_w<F, D, M, 2>(p, s) : launch_dir_w<F, D, M, 0>(p, s);
 }
 
 template <int F, int D>
