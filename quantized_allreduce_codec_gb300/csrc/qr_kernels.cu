@@ -57,8 +57,8 @@ cudaError_t resident_ctas(void (*kern)(Params), int threads, int smem, unsigned 
   return cudaSuccess;
 }
 
-template <int F, int D, int M>
-cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
+template <int F, int D, int M, int WS>
+cudaError_t launch_pipe_w(const PipeParams& p, cudaStream_t s) {
   // Per-device launch geometry, computed once (benign race: same values).
   static int ctas_per_sm[kMaxDevices];
   static int sm_count[kMaxDevices];
@@ -66,7 +66,7 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  auto kern = qr_pipeline_kernel<F, D, M>;
+  auto kern = qr_pipeline_kernel<F, D, M, WS>;
   if (ctas_per_sm[dev] == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesOf<M>);
     if (e != cudaSuccess) return e;
@@ -81,6 +81,14 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   const unsigned long long max_grid = (unsigned long long)sm_count[dev] * ctas_per_sm[dev];
   const unsigned grid = static_cast<unsigned>(p.ntiles < max_grid ? p.ntiles : max_grid);
   return launch_overlapped(kern, grid, kThreads, kSmemBytesOf<M>, s, p);
+}
+
+// Rank count known at compile time where it is fixed or common: 1 for
+// encode-only, 2 for the tp2 case; other W take the general instantiation.
+template <int F, int D, int M>
+cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
+  if (M == MODE_ENCODE) return launch_pipe_w<F, D, M, 1>(p, s);
+  return p.W == 2 ? launch_pipe_w<F, D, M, 2>(p, s) : launch_pipe_w<F, D, M, 0>(p, s);
 }
 
 template <int F, int D, int M, int WS>
