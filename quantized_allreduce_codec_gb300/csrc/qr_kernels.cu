@@ -120,22 +120,28 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
   return launch_overlapped(qr_decode_kernel<F, D>, grid, kDecodeThreads, 0, s, p);
 }
 
-template <int F, int D>
-cudaError_t launch_stg(const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
+template <int F, int D, int WS>
+cudaError_t launch_stg_w(const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
   static unsigned long long cap1[kMaxDevices], cap2[kMaxDevices];
   unsigned long long max1 = 0, max2 = 0;
-  cudaError_t e = resident_ctas(qr_scatter_encode_kernel<F, D>, kStagedThreads, 0, cap1, &max1);
+  cudaError_t e = resident_ctas(qr_scatter_encode_kernel<F, D, WS>, kStagedThreads, 0, cap1, &max1);
   if (e != cudaSuccess) return e;
-  e = resident_ctas(qr_owner_reduce_kernel<F, D>, kStagedThreads, 0, cap2, &max2);
+  e = resident_ctas(qr_owner_reduce_kernel<F, D, WS>, kStagedThreads, 0, cap2, &max2);
   if (e != cudaSuccess) return e;
   const unsigned long long want = (p.nb + kStagedThreads - 1) / kStagedThreads;
-  e = launch_overlapped(qr_scatter_encode_kernel<F, D>, static_cast<unsigned>(want < max1 ? want : max1),
+  e = launch_overlapped(qr_scatter_encode_kernel<F, D, WS>, static_cast<unsigned>(want < max1 ? want : max1),
                         kStagedThreads, 0, s, p);
   if (e != cudaSuccess) return e;
-  e = launch_overlapped(qr_owner_reduce_kernel<F, D>, static_cast<unsigned>(want < max2 ? want : max2),
+  e = launch_overlapped(qr_owner_reduce_kernel<F, D, WS>, static_cast<unsigned>(want < max2 ? want : max2),
                         kStagedThreads, 0, s, p);
   if (e != cudaSuccess) return e;
   return launch_dec<F, D>(dp, s);
+}
+
+// W = 2 has its own instantiation with the rank count known.
+template <int F, int D>
+cudaError_t launch_stg(const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
+  return p.W == 2 ? launch_stg_w<F, D, 2>(p, dp, s) : launch_stg_w<F, D, 0>(p, dp, s);
 }
 
 }  // namespace

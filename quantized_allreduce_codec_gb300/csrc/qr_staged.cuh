@@ -131,25 +131,42 @@ __device__ __forceinline__ void encode_store_block(const float (&x)[32], const B
   if (FmtInfo<F>::asym) zps[blk] = b.z_bits;
 }
 
+// Calls f(r) for the ranks r = 0 .. W-1 in order: fully unrolled when the
+// rank count WS is a compile-time constant, a runtime loop when WS is 0.
+template <int WS, typename Fn>
+__device__ __forceinline__ void for_ranks(int W, Fn&& f) {
+  if constexpr (WS > 0) {
+#pragma unroll
+    for (int r = 0; r < WS; ++r) f(r);
+  } else {
+    for (int r = 0; r < W; ++r) f(r);
+  }
+}
+
+// Number of valid 8-element chunks of block blk: 4 unless the block is the
+// message's ragged last one.  FULL asserts that blk lies wholly inside.
+template <bool FULL>
+__device__ __forceinline__ int valid_chunks(unsigned long long n, unsigned long long blk) {
+  if constexpr (FULL) return 4;
+  const unsigned long long rem = n - blk * 32;
+  return rem >= 32 ? 4 : static_cast<int>(rem / 8);
+}
+
 // Kernel 1: one thread per block; for every rank, load its 64 bytes, encode
-// the block and write it into slot (owner, rank).
-template <int F, int D>
-__global__ void __launch_bounds__(kStagedThreads) qr_scatter_encode_kernel(const __grid_constant__ StagedParams p) {
-  wait_prior_grid();
-  allow_next_grid();
-  const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
-  const int W = p.W;
-  for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
-       blk += stride) {
-    const unsigned long long rem = p.n - blk * 32;
-    const int nvalid = rem >= 32 ? 4 : static_cast<int>(rem / 8);
+// the block and write it into slot (owner, rank).  scatter_block is one
+// block's work; WS is the rank count when it is known at compile time (2)
+// or 0, and FULL (used only with a known WS) that the block is complete.
+template <int F, int D, int WS, bool FULL>
+__device__ __forceinline__ void scatter_block(const StagedParams& p, unsigned long long blk) {
+  const int W = WS ? WS : p.W;
+    const int nvalid = valid_chunks<FULL>(p.n, blk);
     const unsigned long long j = owner_of(blk, p.chunk_nb, W);
     const unsigned long long local = blk - j * p.chunk_nb;
     uint4 next[4];  // the next rank's block, loaded one rank ahead
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       next[k] = k < nvalid ? __ldg(reinterpret_cast<const uint4*>(p.in[0]) + blk * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
-    for (int r = 0; r < W; ++r) {
+    for_ranks<WS>(W, [&](int r) {
       uint8_t* slot = p.stage1 + (j * W + r) * p.slot_bytes;
       uint4 raw[4];
 #pragma unroll
@@ -174,6 +191,24 @@ __global__ void __launch_bounds__(kStagedThreads) qr_scatter_encode_kernel(const
                               reinterpret_cast<uint16_t*>(slot + slot_scales_off<F>(p.chunk_nb)),
                               reinterpret_cast<uint16_t*>(slot + slot_zps_off<F>(p.chunk_nb)), local);
       }
+    });
+}
+
+template <int F, int D, int WS>
+__global__ void __launch_bounds__(kStagedThreads) qr_scatter_encode_kernel(const __grid_constant__ StagedParams p) {
+  wait_prior_grid();
+  allow_next_grid();
+  const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
+  const unsigned long long nb_full = p.n / 32;  // blocks holding 32 elements
+  for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
+       blk += stride) {
+    if constexpr (WS > 0) {
+      if (blk < nb_full)
+        scatter_block<F, D, WS, true>(p, blk);
+      else
+        scatter_block<F, D, WS, false>(p, blk);
+    } else {
+      scatter_block<F, D, 0, false>(p, blk);
     }
   }
 }
@@ -217,22 +252,17 @@ __device__ __forceinline__ void load_slot_block(const uint8_t* slot, unsigned lo
 }
 
 // Kernel 2: one thread per block; the owner decodes the block from its W
-// source slots, sums them in rank order and requantizes into the payload.
-template <int F, int D>
-__global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const __grid_constant__ StagedParams p) {
-  wait_prior_grid();
-  allow_next_grid();
-  const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
-  const int W = p.W;
-  for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
-       blk += stride) {
-    const unsigned long long rem = p.n - blk * 32;
-    const int nvalid = rem >= 32 ? 4 : static_cast<int>(rem / 8);
+// source slots, sums them in rank order and requantizes into the payload
+// (reduce_block: one block; WS and FULL as for scatter_block).
+template <int F, int D, int WS, bool FULL>
+__device__ __forceinline__ void reduce_block(const StagedParams& p, unsigned long long blk) {
+  const int W = WS ? WS : p.W;
+    const int nvalid = valid_chunks<FULL>(p.n, blk);
     const unsigned long long j = owner_of(blk, p.chunk_nb, W);
     const unsigned long long local = blk - j * p.chunk_nb;
     float acc[32];
     if constexpr (!FmtInfo<F>::quant) {
-      for (int r = 0; r < W; ++r) {
+      for_ranks<WS>(W, [&](int r) {
         const uint4* src = reinterpret_cast<const uint4*>(p.stage1 + (j * W + r) * p.slot_bytes + local * 64);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -241,7 +271,7 @@ __global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const _
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc[8 * k + i] = (r == 0) ? y[i] : __fadd_rn(acc[8 * k + i], y[i]);
         }
-      }
+      });
       uint4* dst = reinterpret_cast<uint4*>(p.fp_values) + blk * 4;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
@@ -250,7 +280,7 @@ __global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const _
       uint32_t cw[8], ncw[8];  // this rank's and the next rank's code words
       uint16_t sb = 0, zb = 0, nsb = 0, nzb = 0;
       load_slot_block<F>(p.stage1 + j * W * p.slot_bytes, p.chunk_nb, local, ncw, nsb, nzb);
-      for (int r = 0; r < W; ++r) {
+      for_ranks<WS>(W, [&](int r) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) cw[i] = ncw[i];
         sb = nsb;
@@ -267,7 +297,7 @@ __global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const _
           else
             unpack8_accumulate<F, false>(chunk_code_words<F>(cw, k), b, &acc[8 * k]);
         }
-      }
+      });
       if (nvalid < 4 && !FmtInfo<F>::asym) {  // the symmetric statistic skips invalid chunks as zeros
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -279,6 +309,24 @@ __global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const _
       bool fast;
       const BlockScale b2 = f32_block_scale<F>(acc, nvalid, fast);
       encode_store_block<F>(acc, b2, p.one, fast, nvalid, p.codes, p.scales, p.zps, blk);
+    }
+}
+
+template <int F, int D, int WS>
+__global__ void __launch_bounds__(kStagedThreads) qr_owner_reduce_kernel(const __grid_constant__ StagedParams p) {
+  wait_prior_grid();
+  allow_next_grid();
+  const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
+  const unsigned long long nb_full = p.n / 32;
+  for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
+       blk += stride) {
+    if constexpr (WS > 0) {
+      if (blk < nb_full)
+        reduce_block<F, D, WS, true>(p, blk);
+      else
+        reduce_block<F, D, WS, false>(p, blk);
+    } else {
+      reduce_block<F, D, 0, false>(p, blk);
     }
   }
 }
