@@ -136,6 +136,28 @@ def test_allreduce_parity(oracle_mod, W, dtype, fmt, stages, n, path):
         assert_encoded_equal(wire, o_wire, fmt, n)
 
 
+@pytest.mark.parametrize("W", [2, 4, 8])
+@pytest.mark.parametrize("fmt", [Q8A, Q4A, Q8, Q4])
+@pytest.mark.parametrize("dtype", [F16, BF16])
+def test_offset_blocks_parity(oracle_mod, W, dtype, fmt, path):
+    """Blocks far from zero with small ranges (+-500 + 0.3 N(0,1) per rank):
+    the sums' fp16 zero-points lie many steps above their minima, so the
+    asymmetric requantization must clamp codes at 0 (the clamp-free fast
+    path must not be taken); the symmetric formats get scales set by large,
+    nearly equal magnitudes."""
+    rng = np.random.default_rng(7000 + 11 * W + fmt + 3 * dtype)
+    n = 3 * 8192 + 40
+    sign = np.repeat(rng.choice(np.array([-1.0, 1.0], np.float32), (n + 31) // 32), 32)[:n]
+    xs = [to_bits((sign * 500.0 + 0.3 * rng.standard_normal(n)).astype(np.float32), dtype)
+          for _ in range(W)]
+    for stages in (1, 2):
+        out, wire = gpu_allreduce(dtype, fmt, stages, xs)
+        o_out, o_wire = oracle_mod.allreduce(dtype, fmt, stages, xs)
+        assert_bits_equal(out, o_out)
+        if stages == 2:
+            assert_encoded_equal(wire, o_wire, fmt, n)
+
+
 @pytest.mark.parametrize("fmt", ALL_FORMATS)
 def test_allreduce_without_wire_gives_same_output(oracle_mod, fmt, path):
     rng = np.random.default_rng(5000 + fmt)

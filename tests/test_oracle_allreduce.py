@@ -11,7 +11,7 @@ import torch
 
 from quantized_allreduce_codec_gb300.inputs import (ALL_FORMATS, BF16, F16, FP, FP8, Q4, Q4A,
                                                     Q6, Q8, Q8A, from_bits, to_bits, workloads)
-from test_oracle_codec import BITS, SYM, ASYM, QUANT, e4m3_table, parse
+from test_oracle_codec import BITS, SYM, ASYM, QUANT, e4m3_table, parse, pick
 
 DTYPES = (F16, BF16)
 
@@ -124,6 +124,39 @@ def test_quantized_stages_compose_from_codec(oracle_mod, dtype, fmt, W):
             want = np.float32(np.max(blk) - np.min(blk)) / np.float32(L)
             assert zps[b] == np.float32(np.min(blk)).astype(np.float16).astype(np.float32)
         assert scales[b] == np.float32(want).astype(np.float16).astype(np.float32)
+
+
+@pytest.mark.parametrize("fmt", ASYM)
+def test_asym_requantization_codes_are_bruteforce_nearest(oracle_mod, fmt):
+    """Stage-2 codes of the asymmetric formats, checked one by one: each is
+    the admissible code (0..2^b-1) nearest to (acc - z) * (1/s), ties to
+    even, where acc is the binary32 rank-order sum composed from the codec.
+    The sums sit near 1000 with ranges near 1, so the fp16 zero-point h(min)
+    often lies above the block minimum by many steps (fp16 spacing 0.5 there
+    against a step near 0.004): those codes must clamp to 0.  fp16 inputs
+    never reach this case in stage 1, where the minimum is itself an fp16
+    value and h(min) is exact."""
+    rng = np.random.default_rng(400 + fmt)
+    W, n = 2, 32 * 96
+    x = [to_bits((500.0 + 0.3 * rng.standard_normal(n)).astype(np.float32), F16) for _ in range(W)]
+    acc = None
+    for r in range(W):
+        d = decoded_f32(oracle_mod.quantize(F16, fmt, x[r]), fmt, n)
+        acc = d if acc is None else (acc + d).astype(np.float32)
+    _, wire = oracle_mod.allreduce(F16, fmt, 2, x)
+    codes, scales, zps = parse(wire, fmt, n)
+    L = (1 << BITS[fmt]) - 1
+    cands = np.arange(0, L + 1)
+    below = 0
+    for b in range(n // 32):
+        blk = acc[32 * b:32 * b + 32]
+        assert scales[b] > 0
+        inv = np.float32(1.0) / np.float32(scales[b])
+        v = ((blk - np.float32(zps[b])).astype(np.float32) * inv).astype(np.float32).astype(np.float64)
+        below += int(np.sum(v < -0.5))
+        for i in range(32):
+            assert codes[b, i] == pick(np.abs(v[i] - cands), cands), (b, i, v[i])
+    assert below > 0, "no code needed the lower clamp"
 
 
 @pytest.mark.parametrize("dtype", DTYPES)

@@ -59,6 +59,7 @@ MUTANTS = [
     ("tail stats over all 32", "    for (int i = 1; i < cnt; ++i) {\n      if (x[i] < m) m = x[i];",
      "    for (int i = 1; i < QRO_BLOCK; ++i) {\n      if (x[i] < m) m = x[i];"),
     ("sym absmax ignores sign", "    float ax = fabsf(x[i]);", "    float ax = x[i];"),
+    ("asym lower clamp missing", "      if (r < 0.0f) r = 0.0f;\n", ""),
     ("cast option truncates its result to bf16",
      "    for (size_t i = 0; i < n; ++i) out[i] = qro_f32_to_bf16(qro_f16_to_f32(o16[i]));",
      "    for (size_t i = 0; i < n; ++i) {\n      float f = qro_f16_to_f32(o16[i]);\n      uint32_t u;\n"
@@ -104,6 +105,8 @@ def battery(o):
     yield lambda: TV.test_f16_encode_matches_numpy(o)
     yield lambda: TV.test_bf16_encode_matches_torch(o)
     yield lambda: TV.test_e4m3_encode_matches_torch_in_range(o)
+    for f in (Q8A, Q4A):
+        yield lambda f=f: TA.test_asym_requantization_codes_are_bruteforce_nearest(o, f)
     for f, st in ((FP, 2), (Q4A, 2), (Q8, 1)):
         yield lambda f=f, st=st: TA.test_bf16_cast_option_is_fp16_run_between_library_casts(o, f, st)
 
