@@ -72,11 +72,24 @@ def random_blocks(rng, dtype, nblocks, spread=True):
     return to_bits(x, dtype)
 
 
+def with_saturating_blocks(rng, xb, dtype):
+    """bf16 only: the last two blocks get magnitudes near 2^40 (one of them
+    offset by 2^36 with a small spread), beyond what an fp16 scale or
+    zero-point can hold, so the saturating fp16 rounding of the statistics
+    decides the codes.  fp16 messages are returned unchanged."""
+    if dtype != BF16:
+        return xb
+    x = from_bits(xb, dtype)
+    x[-64:-32] = rng.standard_normal(32).astype(np.float32) * np.float32(2.0 ** 40)
+    x[-32:] = np.float32(2.0 ** 36) + rng.standard_normal(32).astype(np.float32) * np.float32(2.0 ** 30)
+    return to_bits(x, dtype)
+
+
 @pytest.mark.parametrize("dtype", [F16, BF16])
 @pytest.mark.parametrize("fmt", SYM)
 def test_sym_codes_are_bruteforce_nearest(oracle_mod, dtype, fmt):
     rng = np.random.default_rng(100 + fmt)
-    xb = random_blocks(rng, dtype, 64)
+    xb = with_saturating_blocks(rng, random_blocks(rng, dtype, 64), dtype)
     x = from_bits(xb, dtype)
     enc = oracle_mod.quantize(dtype, fmt, xb)
     codes, scales, _ = parse(enc, fmt, x.size)
@@ -100,7 +113,7 @@ def test_sym_codes_are_bruteforce_nearest(oracle_mod, dtype, fmt):
 @pytest.mark.parametrize("fmt", ASYM)
 def test_asym_codes_are_bruteforce_nearest(oracle_mod, dtype, fmt):
     rng = np.random.default_rng(200 + fmt)
-    xb = random_blocks(rng, dtype, 64)
+    xb = with_saturating_blocks(rng, random_blocks(rng, dtype, 64), dtype)
     x = from_bits(xb, dtype)
     x[32:64] += np.float32(3.0)  # a block with a large offset
     xb = to_bits(x, dtype)
@@ -126,7 +139,7 @@ def test_asym_codes_are_bruteforce_nearest(oracle_mod, dtype, fmt):
 @pytest.mark.parametrize("dtype", [F16, BF16])
 def test_fp8_codes_are_bruteforce_nearest(oracle_mod, dtype):
     rng = np.random.default_rng(300)
-    xb = random_blocks(rng, dtype, 64)
+    xb = with_saturating_blocks(rng, random_blocks(rng, dtype, 64), dtype)
     x = from_bits(xb, dtype)
     enc = oracle_mod.quantize(dtype, FP8, xb)
     codes, scales, _ = parse(enc, FP8, x.size)

@@ -60,6 +60,13 @@ MUTANTS = [
      "    for (int i = 1; i < QRO_BLOCK; ++i) {\n      if (x[i] < m) m = x[i];"),
     ("sym absmax ignores sign", "    float ax = fabsf(x[i]);", "    float ax = x[i];"),
     ("asym lower clamp missing", "      if (r < 0.0f) r = 0.0f;\n", ""),
+    ("sym and fp8 scale not saturating", "  bc->s_bits = qro_f32_to_f16_satfinite(ratio);\n  bc->s = qro_f16_to_f32(bc->s_bits);\n  if",
+     "  bc->s_bits = qro_f32_to_f16(ratio);\n  bc->s = qro_f16_to_f32(bc->s_bits);\n  if"),
+    ("asym scale not saturating", "    bc->s_bits = qro_f32_to_f16_satfinite(ratio);\n    bc->z_bits",
+     "    bc->s_bits = qro_f32_to_f16(ratio);\n    bc->z_bits"),
+    ("asym zero-point not saturating", "    bc->z_bits = qro_f32_to_f16_satfinite(m);", "    bc->z_bits = qro_f32_to_f16(m);"),
+    ("more than eight ranks accepted", "  if (W < 1 || W > 8 || !valid_dtype(dtype) || !valid_format(fmt)) return -1;",
+     "  if (W < 1 || W > 16 || !valid_dtype(dtype) || !valid_format(fmt)) return -1;"),
     ("cast option truncates its result to bf16",
      "    for (size_t i = 0; i < n; ++i) out[i] = qro_f32_to_bf16(qro_f16_to_f32(o16[i]));",
      "    for (size_t i = 0; i < n; ++i) {\n      float f = qro_f16_to_f32(o16[i]);\n      uint32_t u;\n"
@@ -72,6 +79,7 @@ MUTANTS = [
 def battery(o):
     """The pin tests, cheapest first, as callables on an oracle object."""
     yield lambda: TC.test_hand_worked_q8_block(o)
+    yield lambda: TA.test_rejects_bad_arguments(o)
     yield lambda: TC.test_packing_known_answer_q6_q4(o)
     yield lambda: TC.test_zero_block_and_tiny_block(o)
     yield lambda: TA.test_signed_zeros_fp_path(o, F16)
@@ -115,7 +123,7 @@ def first_failure(o):
     for i, check in enumerate(battery(o)):
         try:
             check()
-        except (AssertionError, ValueError) as e:
+        except (AssertionError, ValueError, pytest.fail.Exception) as e:  # the last: pytest.raises saw no error
             return i, repr(e)[:120]
     return None
 
