@@ -125,6 +125,18 @@ def _dtype_code(dtype) -> int:
     raise ValueError(f"unsupported dtype {dtype}")
 
 
+def _rank_pointers(inputs, W: int, what: str):
+    """Host array of the W rank pointers, as the C calls read it.  The C side
+    reads exactly W entries, so a list of any other length is refused here
+    instead of being read past its end."""
+    if len(inputs) != W:
+        raise ValueError(f"{what}: {len(inputs)} rank buffers given for W={W}")
+    if not inputs:
+        return None
+    ptrs = (ctypes.c_void_p * len(inputs))(*[_addr(x) for x in inputs])
+    return ctypes.cast(ptrs, ctypes.c_void_p)
+
+
 def qr_status_string(status: int) -> str:
     return lib().qr_status_string(status).decode()
 
@@ -148,9 +160,8 @@ def qr_dequantize(dtype, fmt: int, enc, n: int, out, stream=None) -> None:
 def qr_allreduce_emulated(W: int, dtype, fmt: int, stages: int, inputs, n: int, out,
                           wire=None, stream=None) -> None:
     """Emulated allreduce of W rank messages (list of W tensors / addresses)."""
-    ptrs = (ctypes.c_void_p * max(len(inputs), 1))(*[_addr(x) for x in inputs])
-    _check(lib().qr_allreduce_emulated(W, _dtype_code(dtype), fmt, stages,
-                                       ctypes.cast(ptrs, ctypes.c_void_p) if inputs else None, n,
+    ptrs = _rank_pointers(inputs, W, "qr_allreduce_emulated")
+    _check(lib().qr_allreduce_emulated(W, _dtype_code(dtype), fmt, stages, ptrs, n,
                                        _addr(out), _addr(wire), _stream(stream)),
            "qr_allreduce_emulated")
 
@@ -187,9 +198,8 @@ def qr_stage1_bytes(W: int, fmt: int, n: int) -> int:
 def qr_allreduce_staged(W: int, dtype, fmt: int, inputs, n: int, out, wire, stage1,
                         stream=None) -> None:
     """Two-stage allreduce with the stage-1 exchange materialised in `stage1`."""
-    ptrs = (ctypes.c_void_p * max(len(inputs), 1))(*[_addr(x) for x in inputs])
-    _check(lib().qr_allreduce_staged(W, _dtype_code(dtype), fmt,
-                                     ctypes.cast(ptrs, ctypes.c_void_p) if inputs else None, n,
+    ptrs = _rank_pointers(inputs, W, "qr_allreduce_staged")
+    _check(lib().qr_allreduce_staged(W, _dtype_code(dtype), fmt, ptrs, n,
                                      _addr(out), _addr(wire), _addr(stage1), _stream(stream)),
            "qr_allreduce_staged")
 
@@ -204,9 +214,8 @@ def qr_allreduce_staged_noalloc(W: int, dtype, fmt: int, inputs, n: int, out, wi
     example while a CUDA graph is being captured).  Messages needing more
     than NOALLOC_SCRATCH_BYTES of stage-1 space raise QR_ERR_SCRATCH; calls
     that overlap on the GPU share the array and race."""
-    ptrs = (ctypes.c_void_p * max(len(inputs), 1))(*[_addr(x) for x in inputs])
-    _check(lib().qr_allreduce_staged_noalloc(W, _dtype_code(dtype), fmt,
-                                             ctypes.cast(ptrs, ctypes.c_void_p) if inputs else None, n,
+    ptrs = _rank_pointers(inputs, W, "qr_allreduce_staged_noalloc")
+    _check(lib().qr_allreduce_staged_noalloc(W, _dtype_code(dtype), fmt, ptrs, n,
                                              _addr(out), _addr(wire), _stream(stream)),
            "qr_allreduce_staged_noalloc")
 
@@ -238,9 +247,8 @@ def qr_allreduce_host(W: int, dtype, fmt: int, stages: int, host_inputs, n: int,
         if isinstance(workspace, int):
             raise ValueError("workspace_bytes is required with a raw workspace address")
         workspace_bytes = workspace.numel() * workspace.element_size()
-    ptrs = (ctypes.c_void_p * max(len(host_inputs), 1))(*[_addr(x) for x in host_inputs])
-    _check(lib().qr_allreduce_host(W, _dtype_code(dtype), fmt, stages,
-                                   ctypes.cast(ptrs, ctypes.c_void_p) if host_inputs else None, n,
+    ptrs = _rank_pointers(host_inputs, W, "qr_allreduce_host")
+    _check(lib().qr_allreduce_host(W, _dtype_code(dtype), fmt, stages, ptrs, n,
                                    _addr(host_out), _addr(host_wire), _addr(workspace), workspace_bytes,
                                    chunk_elems, _stream(stream)),
            "qr_allreduce_host")

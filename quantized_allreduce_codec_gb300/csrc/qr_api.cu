@@ -187,15 +187,74 @@ size_t host_chunk_buffer_bytes(int W, int fmt, size_t chunk) {
 }  // namespace
 
 unsigned* device_error_word() {
-  static unsigned* addr[kMaxDevices];
+  // one atomic pointer per device: racing first calls each look the address
+  // up and publish the same value
+  static std::atomic<unsigned*> addr[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!addr[dev]) {
+  unsigned* a = addr[dev].load(std::memory_order_acquire);
+  if (!a) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_qr_error_flags) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<unsigned*>(p);
+    if (cudaGetSymbolAddress(&p, g_qr_error_flags) != cudaSuccess || !p) return nullptr;
+    a = static_cast<unsigned*>(p);
+    addr[dev].store(a, std::memory_order_release);
   }
-  return addr[dev];
+  return a;
+}
+
+qr_status staged_check_args(int W, int dt, int fmt, size_t n) {
+  if (!valid_dtype(dt)) return QR_ERR_DTYPE;
+  if (!valid_format(fmt)) return QR_ERR_FORMAT;
+  if (W != 1 && W != 2 && W != 4 && W != 8) return QR_ERR_WORLD;
+  return check_size(n);
+}
+
+qr_status staged_check_buffers(int W, int fmt, const void* const* inputs, size_t n, const void* out,
+                               const void* wire, const void* stage1) {
+  for (int r = 0; r < W; ++r)
+    if (!inputs[r]) return QR_ERR_NULL;
+  if (!aligned16(out) || !aligned16(wire) || (stage1 && !aligned16(stage1))) return QR_ERR_ALIGN;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(inputs[r])) return QR_ERR_ALIGN;
+  const qr_format fm = static_cast<qr_format>(fmt);
+  const size_t msg = n * 2, wbytes = qr_encoded_bytes(fm, n), sbytes = stage1 ? qr_stage1_bytes(W, fm, n) : 0;
+  for (int r = 0; r < W; ++r)
+    if (overlap(inputs[r], msg, out, msg) || overlap(inputs[r], msg, wire, wbytes) ||
+        overlap(inputs[r], msg, stage1, sbytes))
+      return QR_ERR_OVERLAP;
+  if (overlap(out, msg, wire, wbytes) || overlap(out, msg, stage1, sbytes) || overlap(wire, wbytes, stage1, sbytes))
+    return QR_ERR_OVERLAP;
+  return QR_OK;
+}
+
+qr_status staged_launch(int W, int dt, int fmt, const void* const* inputs, size_t n, void* out, void* wire,
+                        uint8_t* stage1, cudaStream_t s) {
+  StagedParams p;
+  std::memset(&p, 0, sizeof p);
+  p.one = 1.0f;
+  for (int r = 0; r < W; ++r) p.in[r] = inputs[r];
+  p.W = W;
+  p.n = n;
+  p.nb = (n + 31) / 32;
+  size_t chunk_nb, slot_bytes;
+  staged_geometry(W, fmt, n, &chunk_nb, &slot_bytes);
+  p.chunk_nb = chunk_nb;
+  p.slot_bytes = slot_bytes;
+  p.stage1 = stage1;
+  encoded_regions(fmt, n, wire, &p.codes, &p.scales, &p.zps, &p.fp_values);
+
+  DecodeParams dp;
+  std::memset(&dp, 0, sizeof dp);
+  dp.codes = p.codes;
+  dp.scales = p.scales;
+  dp.zps = p.zps;
+  dp.fp_values = p.fp_values;
+  dp.out = out;
+  dp.n = n;
+  dp.nb = p.nb;
+  dp.err = device_error_word();
+  if (!dp.err) return QR_ERR_CUDA;
+  return to_status(dispatch_staged(fmt, dt, p, dp, s));
 }
 
 }  // namespace qr
@@ -333,51 +392,13 @@ qr_status qr_allreduce_staged(int W, qr_dtype dt, qr_format fmt, const void* con
                               void* wire, void* stage1, void* stream) {
   const int f = static_cast<int>(fmt), d = static_cast<int>(dt);
   if (n && (!inputs || !out || !wire || !stage1)) return QR_ERR_NULL;
-  if (!valid_dtype(d)) return QR_ERR_DTYPE;
-  if (!valid_format(f)) return QR_ERR_FORMAT;
-  if (W != 1 && W != 2 && W != 4 && W != 8) return QR_ERR_WORLD;
-  qr_status st = check_size(n);
+  qr_status st = staged_check_args(W, d, f, n);
   if (st != QR_OK) return st;
   if (n == 0) return QR_OK;
-  for (int r = 0; r < W; ++r)
-    if (!inputs[r]) return QR_ERR_NULL;
-  if (!aligned16(out) || !aligned16(wire) || !aligned16(stage1)) return QR_ERR_ALIGN;
-  for (int r = 0; r < W; ++r)
-    if (!aligned16(inputs[r])) return QR_ERR_ALIGN;
-  const size_t msg = n * 2, wbytes = qr_encoded_bytes(fmt, n), sbytes = qr_stage1_bytes(W, fmt, n);
-  for (int r = 0; r < W; ++r)
-    if (overlap(inputs[r], msg, out, msg) || overlap(inputs[r], msg, wire, wbytes) ||
-        overlap(inputs[r], msg, stage1, sbytes))
-      return QR_ERR_OVERLAP;
-  if (overlap(out, msg, wire, wbytes) || overlap(out, msg, stage1, sbytes) || overlap(wire, wbytes, stage1, sbytes))
-    return QR_ERR_OVERLAP;
-
-  StagedParams p;
-  std::memset(&p, 0, sizeof p);
-  p.one = 1.0f;
-  for (int r = 0; r < W; ++r) p.in[r] = inputs[r];
-  p.W = W;
-  p.n = n;
-  p.nb = (n + 31) / 32;
-  size_t chunk_nb, slot_bytes;
-  staged_geometry(W, f, n, &chunk_nb, &slot_bytes);
-  p.chunk_nb = chunk_nb;
-  p.slot_bytes = slot_bytes;
-  p.stage1 = static_cast<uint8_t*>(stage1);
-  encoded_regions(f, n, wire, &p.codes, &p.scales, &p.zps, &p.fp_values);
-
-  DecodeParams dp;
-  std::memset(&dp, 0, sizeof dp);
-  dp.codes = p.codes;
-  dp.scales = p.scales;
-  dp.zps = p.zps;
-  dp.fp_values = p.fp_values;
-  dp.out = out;
-  dp.n = n;
-  dp.nb = p.nb;
-  dp.err = device_error_word();
-  if (!dp.err) return QR_ERR_CUDA;
-  return to_status(dispatch_staged(f, d, p, dp, static_cast<cudaStream_t>(stream)));
+  st = staged_check_buffers(W, f, inputs, n, out, wire, stage1);
+  if (st != QR_OK) return st;
+  return staged_launch(W, d, f, inputs, n, out, wire, static_cast<uint8_t*>(stage1),
+                       static_cast<cudaStream_t>(stream));
 }
 
 size_t qr_host_workspace_bytes(int W, qr_format fmt, size_t chunk_elems) {

@@ -1,6 +1,8 @@
 // qr_kernels.cu -- kernel instantiations and launchers for ONE format,
 // selected at compile time with -DQR_FMT=<n> (the build compiles this file
 // once per format, in parallel).
+#include <atomic>
+
 #include "qr_launch.h"
 
 #ifndef QR_FMT
@@ -37,48 +39,48 @@ cudaError_t launch_overlapped(void (*kern)(Params), unsigned grid, unsigned bloc
 // CTAs of `kern` that are resident on the current device at once (SMs x
 // CTAs per SM at this block size and shared memory), computed once per
 // device; grid-stride kernels are launched with at most this many, so every
-// CTA starts at once and none waits for a second wave.
+// CTA starts at once and none waits for a second wave.  The cache is one
+// atomic word per device: a thread sees either 0 (and computes the same
+// value itself) or the complete value, never a half-written one.
 template <typename Params>
-cudaError_t resident_ctas(void (*kern)(Params), int threads, int smem, unsigned long long* cache,
+cudaError_t resident_ctas(void (*kern)(Params), int threads, int smem, std::atomic<unsigned long long>* cache,
                           unsigned long long* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (cache[dev] == 0) {
+  unsigned long long v = cache[dev].load(std::memory_order_acquire);
+  if (v == 0) {
     int sms = 0, occ = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
     if (e != cudaSuccess) return e;
-    cache[dev] = static_cast<unsigned long long>(sms) * static_cast<unsigned long long>(occ > 0 ? occ : 1);
+    v = static_cast<unsigned long long>(sms) * static_cast<unsigned long long>(occ > 0 ? occ : 1);
+    cache[dev].store(v, std::memory_order_release);
   }
-  *out = cache[dev];
+  *out = v;
   return cudaSuccess;
 }
 
 template <int F, int D, int M, int WS>
 cudaError_t launch_pipe_w(const PipeParams& p, cudaStream_t s) {
-  // Per-device launch geometry, computed once (benign race: same values).
-  static int ctas_per_sm[kMaxDevices];
-  static int sm_count[kMaxDevices];
+  // Resident CTAs of this instantiation on each device, computed once per
+  // device after its shared-memory limit is raised (resident_ctas' atomic
+  // cache: the attribute is set before the value is published).
+  static std::atomic<unsigned long long> cap[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   auto kern = qr_pipeline_kernel<F, D, M, WS>;
-  if (ctas_per_sm[dev] == 0) {
+  if (cap[dev].load(std::memory_order_acquire) == 0) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesOf<M>);
     if (e != cudaSuccess) return e;
-    int sms = 0, occ = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kSmemBytesOf<M>);
-    if (e != cudaSuccess) return e;
-    sm_count[dev] = sms;
-    ctas_per_sm[dev] = occ > 0 ? occ : 1;
   }
-  const unsigned long long max_grid = (unsigned long long)sm_count[dev] * ctas_per_sm[dev];
+  unsigned long long max_grid = 0;
+  e = resident_ctas(kern, kThreads, kSmemBytesOf<M>, cap, &max_grid);
+  if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.ntiles < max_grid ? p.ntiles : max_grid);
   return launch_overlapped(kern, grid, kThreads, kSmemBytesOf<M>, s, p);
 }
@@ -93,7 +95,7 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
 
 template <int F, int D, int M, int WS>
 cudaError_t launch_dir_w(const PipeParams& p, cudaStream_t s) {
-  static unsigned long long cap[kMaxDevices];
+  static std::atomic<unsigned long long> cap[kMaxDevices];
   unsigned long long max_grid = 0;
   cudaError_t e = resident_ctas(qr_direct_kernel<F, D, M, WS>, kDirectThreads, 0, cap, &max_grid);
   if (e != cudaSuccess) return e;
@@ -110,7 +112,7 @@ cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
 
 template <int F, int D>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
-  static unsigned long long cap[kMaxDevices];
+  static std::atomic<unsigned long long> cap[kMaxDevices];
   unsigned long long max_grid = 0;
   cudaError_t e = resident_ctas(qr_decode_kernel<F, D>, kDecodeThreads, 0, cap, &max_grid);
   if (e != cudaSuccess) return e;
@@ -122,7 +124,7 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
 
 template <int F, int D, int WS>
 cudaError_t launch_stg_w(const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
-  static unsigned long long cap1[kMaxDevices], cap2[kMaxDevices];
+  static std::atomic<unsigned long long> cap1[kMaxDevices], cap2[kMaxDevices];
   unsigned long long max1 = 0, max2 = 0;
   cudaError_t e = resident_ctas(qr_scatter_encode_kernel<F, D, WS>, kStagedThreads, 0, cap1, &max1);
   if (e != cudaSuccess) return e;

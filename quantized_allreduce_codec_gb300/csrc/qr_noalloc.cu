@@ -21,7 +21,6 @@
 
 #include <atomic>
 #include <cstdint>
-#include <cstring>
 
 #include "qr.h"
 #include "qr_launch.h"
@@ -50,26 +49,6 @@ uint8_t* scratch_address() {
   return p;
 }
 
-bool is_asym_fmt(int f) { return f == FMT_Q8A || f == FMT_Q4A; }
-
-cudaError_t launch_staged(int fmt, int dt, const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
-  switch (fmt) {
-    case 0: return launch_staged_fmt_0(dt, p, dp, s);
-    case 1: return launch_staged_fmt_1(dt, p, dp, s);
-    case 2: return launch_staged_fmt_2(dt, p, dp, s);
-    case 3: return launch_staged_fmt_3(dt, p, dp, s);
-    case 4: return launch_staged_fmt_4(dt, p, dp, s);
-    case 5: return launch_staged_fmt_5(dt, p, dp, s);
-    case 6: return launch_staged_fmt_6(dt, p, dp, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
-  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return na && nb && x < y + nb && y < x + na;
-}
-
 }  // namespace
 }  // namespace qr
 
@@ -79,59 +58,15 @@ extern "C" qr_status qr_allreduce_staged_noalloc(int W, qr_dtype dt, qr_format f
                                                  size_t n, void* out, void* wire, void* stream) {
   const int f = static_cast<int>(fmt), d = static_cast<int>(dt);
   if (n && (!inputs || !out || !wire)) return QR_ERR_NULL;
-  if (d != DT_F16 && d != DT_BF16) return QR_ERR_DTYPE;
-  if (f < FMT_FP || f > FMT_Q4A) return QR_ERR_FORMAT;
-  if (W != 1 && W != 2 && W != 4 && W != 8) return QR_ERR_WORLD;
-  if (n > QR_MAX_ELEMS || (n * 2) % 16 != 0) return QR_ERR_SIZE;
+  qr_status st = staged_check_args(W, d, f, n);
+  if (st != QR_OK) return st;
   if (n == 0) return QR_OK;
-  const size_t need = qr_stage1_bytes(W, fmt, n);
-  if (need > kNoAllocScratchBytes) return QR_ERR_SCRATCH;
-  for (int r = 0; r < W; ++r)
-    if (!inputs[r]) return QR_ERR_NULL;
-  auto aligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (!aligned(out) || !aligned(wire)) return QR_ERR_ALIGN;
-  for (int r = 0; r < W; ++r)
-    if (!aligned(inputs[r])) return QR_ERR_ALIGN;
-  const size_t msg = n * 2, wbytes = qr_encoded_bytes(fmt, n);
-  for (int r = 0; r < W; ++r)
-    if (overlaps(inputs[r], msg, out, msg) || overlaps(inputs[r], msg, wire, wbytes)) return QR_ERR_OVERLAP;
-  if (overlaps(out, msg, wire, wbytes)) return QR_ERR_OVERLAP;
-
+  // qr_stage1_bytes is the size staged_launch lays the slots out in, so this
+  // bound is exactly what the kernels write into the array
+  if (qr_stage1_bytes(W, fmt, n) > kNoAllocScratchBytes) return QR_ERR_SCRATCH;
+  st = staged_check_buffers(W, f, inputs, n, out, wire, nullptr);
+  if (st != QR_OK) return st;
   uint8_t* scratch = scratch_address();
   if (!scratch) return QR_ERR_CUDA;
-  // Same geometry and regions as qr_allreduce_staged (see qr_stage1_bytes).
-  const size_t nb = (n + 31) / 32;
-  const size_t chunk_nb = (nb + W - 1) / W;
-  const size_t per_block =
-      f == FMT_FP ? 64 : 32 * static_cast<size_t>(f == FMT_Q6 ? 6 : (f == FMT_Q4 || f == FMT_Q4A) ? 4 : 8) / 8 + 2 +
-                             (is_asym_fmt(f) ? 2 : 0);
-  StagedParams p;
-  std::memset(&p, 0, sizeof p);
-  p.one = 1.0f;
-  for (int r = 0; r < W; ++r) p.in[r] = inputs[r];
-  p.W = W;
-  p.n = n;
-  p.nb = nb;
-  p.chunk_nb = chunk_nb;
-  p.slot_bytes = (chunk_nb * per_block + 15) / 16 * 16;
-  p.stage1 = scratch;
-  uint8_t* wb = static_cast<uint8_t*>(wire);
-  if (f == FMT_FP) {
-    p.fp_values = static_cast<uint16_t*>(wire);
-  } else {
-    const size_t cb = per_block - 2 - (is_asym_fmt(f) ? 2 : 0);
-    p.codes = wb;
-    p.scales = reinterpret_cast<uint16_t*>(wb + nb * cb);
-    if (is_asym_fmt(f)) p.zps = reinterpret_cast<uint16_t*>(wb + nb * cb + 2 * nb);
-  }
-  DecodeParams dp;
-  std::memset(&dp, 0, sizeof dp);
-  dp.codes = p.codes;
-  dp.scales = p.scales;
-  dp.zps = p.zps;
-  dp.fp_values = p.fp_values;
-  dp.out = out;
-  dp.n = n;
-  dp.nb = nb;
-  return launch_staged(f, d, p, dp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? QR_OK : QR_ERR_CUDA;
+  return staged_launch(W, d, f, inputs, n, out, wire, scratch, static_cast<cudaStream_t>(stream));
 }

@@ -202,3 +202,60 @@ def test_host_entry_argument_errors(L):
     assert _host(2, 0, 1, 2, [ha, hb], 64, ha + 100, None, **ok) == 8       # out overlaps an input
     assert _host(2, 0, 1, 2, [ha, hb], 64, hc, hb + 2, **ok) == 8           # wire overlaps an input
     assert _host(2, 0, 1, 2, [ha, hb], 64, hc, hc + 64, **ok) == 8          # wire overlaps out
+
+
+def test_noalloc_scratch_size_agrees_with_header():
+    text = open(os.path.join(ROOT, "include", "qr.h")).read()
+    m = re.search(r"#define\s+QR_NOALLOC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m, "QR_NOALLOC_SCRATCH_BYTES not found in include/qr.h"
+    assert qr.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def _staged(W, dt, fmt, inputs, n, out, wire, stage1):
+    arr = (ctypes.c_void_p * max(len(inputs), 1))(*inputs)
+    return qr.lib().qr_allreduce_staged(W, dt, fmt, ctypes.cast(arr, ctypes.c_void_p), n, out, wire, stage1, None)
+
+
+def _noalloc(W, dt, fmt, inputs, n, out, wire):
+    arr = (ctypes.c_void_p * max(len(inputs), 1))(*inputs)
+    return qr.lib().qr_allreduce_staged_noalloc(W, dt, fmt, ctypes.cast(arr, ctypes.c_void_p), n, out, wire, None)
+
+
+def test_staged_entries_share_argument_checks(L):
+    # both staged entry points validate the same way; the one without a
+    # stage-1 argument adds the bound on its built-in array.  Every case
+    # below is refused on the host, before any CUDA call.
+    D = 0x8000000
+    ok_in = [A, B]
+    for call in (lambda *a: _staged(*a, D), _noalloc):
+        assert call(2, 0, 1, ok_in, 0, None, None) == 0                  # empty message
+        assert call(2, 0, 1, ok_in, 64, C, None) == 1                    # no wire
+        assert call(2, 0, 1, [A, 0], 64, C, C + 4096) == 1              # NULL rank pointer
+        assert call(2, 3, 1, ok_in, 64, C, C + 4096) == 2               # dtype (no cast option here)
+        assert call(2, 2, 1, ok_in, 64, C, C + 4096) == 2
+        assert call(2, 0, 7, ok_in, 64, C, C + 4096) == 3               # format
+        assert call(3, 0, 1, [A, B, A], 64, C, C + 4096) == 4           # W
+        assert call(2, 0, 1, ok_in, 60, C, C + 4096) == 6               # not % 16 bytes
+        assert call(2, 0, 1, [A + 2, B], 64, C, C + 4096) == 7          # alignment
+        assert call(2, 0, 1, ok_in, 64, C, C + 4100) == 7
+        assert call(2, 0, 1, ok_in, 64, A + 64, C + 4096) == 8          # out overlaps an input
+        assert call(2, 0, 1, ok_in, 64, C, C + 64) == 8                 # wire overlaps out
+    assert _staged(2, 0, 1, ok_in, 64, C, C + 4096, None) == 1          # no stage-1 buffer
+    assert _staged(2, 0, 1, ok_in, 64, C, C + 4096, D + 8) == 7         # stage-1 alignment
+    assert _staged(2, 0, 1, ok_in, 64, C, C + 4096, C + 32) == 8        # stage 1 overlaps out
+    n = 8 << 20  # W=2 Q8: about 17.8 MB of stage-1 space, beyond the built-in array
+    assert qr.qr_stage1_bytes(2, 1, n) > qr.NOALLOC_SCRATCH_BYTES
+    assert _noalloc(2, 0, 1, ok_in, n, C, C + (64 << 20)) == 11          # QR_ERR_SCRATCH
+
+
+def test_wrappers_refuse_a_rank_list_of_the_wrong_length(L):
+    # the C side reads exactly W pointers; the binding never hands it fewer
+    with pytest.raises(ValueError, match="rank buffers"):
+        qr.qr_allreduce_emulated(2, qr.F16, qr.QR_Q8, 2, [A], 64, C)
+    with pytest.raises(ValueError, match="rank buffers"):
+        qr.qr_allreduce_staged(4, qr.F16, qr.QR_Q8, [A, B], 64, C, C + 4096, 0x8000000)
+    with pytest.raises(ValueError, match="rank buffers"):
+        qr.qr_allreduce_staged_noalloc(8, qr.F16, qr.QR_Q8, [A, B, C], 64, C, C + 4096)
+    with pytest.raises(ValueError, match="rank buffers"):
+        qr.qr_allreduce_host(2, qr.F16, qr.QR_Q8, 2, [A, B, C], 64, C, None, workspace=0x8000000,
+                             workspace_bytes=1 << 30)
