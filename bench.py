@@ -2,24 +2,26 @@
 """Benchmark of the emulated quick-allreduce data path on one GB300 (or N
 independent replicas, one per GPU).
 
-One step = one pass of the whole hot path over the tp2 workload of the vLLM
-PR #18473 timing table at its largest size: W=2 emulated ranks, fp16,
-64 MiB per rank, N(0,1), in the table's six kernels -- FP one-stage, FP
-two-stage, FP8, Q8, Q6 and Q4 two-stage (every two-stage call also writes
-its stage-2 payload).  Inputs are resident in HBM; L2 is flushed before every timed call,
-outside the timed events: a write of at least twice its size, then a read
-of a second buffer of that size, so that the flush leaves no dirty lines to
-be written back during the timed call.
+One step = one pass of the whole hot path over the largest workload that
+fits one GPU: W=8 emulated ranks, fp16, a per-rank tensor of 8192 x 8192
+(128 MiB; 1 GiB of inputs per call), N(0,1) with 0.1 % of the elements
+scaled by 50 -- a 70B-class tensor-parallel prefill hidden state -- through
+every format (FP, FP8, Q8, Q6, Q4, Q8A, Q4A), one-stage and two-stage: 14
+calls, every two-stage call also writing its stage-2 payload.  Inputs are
+resident in HBM and larger than L2; L2 is also flushed before every timed
+call, outside the timed events: a write of at least twice its size, then a
+read of a second buffer of that size, so that the flush leaves no dirty
+lines to be written back during the timed call.
 
 metric: GB/s per rank-message = sum of per-rank message bytes (n*2) over
 the calls / their device time.  The timed region is K replays of a CUDA
 graph holding one step (each call preceded by its L2 flush), timed with
 CUDA events; the same graph without the qr calls is replayed K times and
-its time subtracted.  Eager per-call event times are reported beside it
-(they include a ~4 us launch gap that even an empty kernel shows).  The JSON line also carries the HBM roofline of the fused
-two-stage quantized kernel, the oracle's CPU rate on a bounded sample, an
-end-to-end rate through the C ABI with host buffers, a size sweep, and the
-other workloads.
+its time subtracted.  The JSON line also carries the HBM roofline of the
+fused two-stage quantized launches, a read-heavy streaming reference timed
+the same way, the oracle's CPU rate on a bounded sample, an end-to-end rate
+through the C ABI with host buffers, the tp2 size sweep of vLLM PR #18473's
+timing table (W=2, fp16, 4 KiB .. 128 MiB) and the other workloads.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 N > 1 is launched with torchrun; each rank runs the same workload on its
@@ -42,13 +44,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from quantized_allreduce_codec_gb300.inputs import (BF16, F16, FORMAT_NAMES, FP, FP8, Q4,  # noqa: E402
-                                                    Q4A, Q6, Q8, Q8A, from_bits, sweep_sizes_bytes,
-                                                    sweep_workload, workloads, Workload)
+from quantized_allreduce_codec_gb300.inputs import (ALL_FORMATS, BF16, DTYPE_NAMES, F16,  # noqa: E402
+                                                    FORMAT_NAMES, FP, FP8, Q4, Q4A, Q6, Q8, Q8A,
+                                                    from_bits, sweep_sizes_bytes, sweep_workload,
+                                                    workloads, Workload)
 
 METRIC = "emulated quick-allreduce GB/s per rank-message and % of HBM roofline, 1×GB300"
-STEP_CALLS = [(FP, 1), (FP, 2), (FP8, 2), (Q8, 2), (Q6, 2), (Q4, 2)]  # the tp2 table's kernels
-BENCH_BYTES = 64 << 20
+HEADLINE = 5  # workloads()[5]: W=8, fp16, 8192 x 8192 per rank, 0.1 % outliers x50
+STEP_CALLS = [(f, s) for f in ALL_FORMATS for s in (1, 2)]  # every format, one- and two-stage
+TP2_CALLS = [(FP, 1), (FP, 2), (FP8, 2), (Q8, 2), (Q6, 2), (Q4, 2)]  # the tp2 table's kernels
+TP2_BYTES = 64 << 20
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 CODE_BITS = {Q8: 8, Q6: 6, Q4: 4, FP8: 8, Q8A: 8, Q4A: 4}
@@ -262,6 +267,94 @@ def recorded_traffic(kernel_source: str):
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
+def headline_config(wl: Workload, world: int) -> dict:
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": f"{wl.name}: W={wl.W} emulated ranks, {DTYPE_NAMES[wl.dtype]}, per-rank tensor "
+                        f"[8192 x 8192] ({wl.n} elements, {wl.n * 2 >> 20} MiB), N(0,1) with 0.1% of the "
+                        f"elements x50 (seed {1000 * wl.key}+r); one step = {len(STEP_CALLS)} calls: "
+                        "FP, FP8, Q8, Q6, Q4, Q8A, Q4A, each one-stage and two-stage (two-stage calls write "
+                        "their stage-2 payload)",
+            "W": wl.W, "dtype": DTYPE_NAMES[wl.dtype], "per_rank_elems": wl.n, "per_rank_bytes": wl.n * 2,
+            "calls_per_step": len(STEP_CALLS),
+            "l2": "inputs (W x 128 MiB per call) larger than the 126 MiB L2; on the GPU, L2 also flushed before "
+                  "every timed call, outside the timed events (a 256 MiB write, then a 256 MiB read of a "
+                  "second buffer)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, W ranks emulated in HBM"}
+
+
+def workload_inputs(wl: Workload) -> list:
+    """The workload's rank messages (uint16 bits), ranks drawn in parallel
+    host threads (each rank has its own seeded generator)."""
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(wl.W, host_threads())) as ex:
+        return list(ex.map(wl.rank_bits, range(wl.W)))
+
+
+def sample_block_elems(n: int, count: int, seed: int) -> np.ndarray:
+    """Element indices of `count` distinct 32-element blocks, sorted."""
+    rng = np.random.default_rng(seed)
+    blocks = np.sort(rng.choice(n // 32, min(count, n // 32), replace=False))
+    return (blocks[:, None] * 32 + np.arange(32)[None, :]).reshape(-1)
+
+
+class GpuTimer:
+    """Device time of a sequence of calls: CUDA graphs of [L2 flush, call]
+    pairs replayed and timed with CUDA events on the replaying stream, minus
+    the same graph of flushes alone."""
+
+    def __init__(self, dev):
+        import torch
+        self.torch = torch
+        props = torch.cuda.get_device_properties(dev)
+        self.l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
+        self.flush_buf = torch.empty(max(2 * self.l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+        self.clean_buf = torch.ones(self.flush_buf.numel(), dtype=torch.float32, device=dev)
+        self.cap_stream = torch.cuda.Stream(device=dev)
+        self.flush_graphs = {}
+
+    def flush(self):
+        # write more than twice the L2 (evicts the inputs), then read a second
+        # buffer of that size so the dirty lines of the write are written back
+        # here rather than inside the next timed call
+        self.flush_buf.fill_(1)
+        self.clean_buf.sum()
+
+    def capture(self, fn):
+        g = self.torch.cuda.CUDAGraph()
+        self.torch.cuda.synchronize()
+        with self.torch.cuda.graph(g, stream=self.cap_stream):
+            fn()
+        self.torch.cuda.synchronize()
+        return g
+
+    def replay_time(self, g, reps):
+        torch = self.torch
+        s = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(reps):
+            g.replay()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e-3
+
+    def per_call_seconds(self, fn, reps):
+        """Device time of fn per call: [flush, fn] x reps minus [flush] x reps
+        (the median of three replays of each)."""
+        fn()  # eager first call: any one-time set-up happens outside capture
+        self.torch.cuda.synchronize()
+        g1 = self.capture(lambda: [(self.flush(), fn()) for _ in range(reps)])
+        if reps not in self.flush_graphs:
+            self.flush_graphs[reps] = self.capture(lambda: [self.flush() for _ in range(reps)])
+        g0 = self.flush_graphs[reps]
+        for g in (g1, g0):
+            g.replay()
+        t1 = statistics.median(self.replay_time(g1, 1) for _ in range(3))
+        t0 = statistics.median(self.replay_time(g0, 1) for _ in range(3))
+        del g1
+        return max((t1 - t0) / reps, 1e-9)
+
+
 def run_ours(args):
     import torch
 
@@ -276,31 +369,20 @@ def run_ours(args):
     dist_barrier()
     qr.lib()
     dev = torch.device("cuda", local)
-
     props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
-    flush_buf = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
-    clean_buf = torch.ones(flush_buf.numel(), dtype=torch.float32, device=dev)
+    timer = GpuTimer(dev)
+    flush = timer.flush
 
-    def flush():
-        # write more than twice the L2 (evicts the inputs), then read a second
-        # buffer of that size so the dirty lines of the write are written back
-        # here rather than inside the next timed call
-        flush_buf.fill_(1)
-        clean_buf.sum()
-
-    wl = sweep_workload(BENCH_BYTES)
+    wl = workloads()[HEADLINE]
     n, W = wl.n, wl.W
-    host = wl.inputs()
+    host = workload_inputs(wl)
     ins = [torch.from_numpy(x.view(np.int16)).to(dev) for x in host]
     out = torch.empty(n, dtype=torch.int16, device=dev)
-    wires = {f: torch.empty(encoded_bytes(f, n), dtype=torch.uint8, device=dev) for f, _ in STEP_CALLS}
+    wires = {f: torch.empty(encoded_bytes(f, n), dtype=torch.uint8, device=dev) for f in ALL_FORMATS}
 
-    def call(fmt, stages, inputs=None, nn=n, o=out):
+    def call(fmt, stages):
         # stream=None: torch's current stream (the capture stream inside a graph)
-        inputs = ins if inputs is None else inputs
-        qr.qr_allreduce_emulated(len(inputs), wl.dtype, fmt, stages, inputs, nn, o,
-                                 wires[fmt] if stages == 2 else None, None)
+        qr.qr_allreduce_emulated(W, wl.dtype, fmt, stages, ins, n, out, wires[fmt] if stages == 2 else None, None)
 
     # warm-up, eager (also first-call set-up of every instantiation used)
     for _ in range(args.warmup):
@@ -311,51 +393,13 @@ def run_ours(args):
     if qr.qr_device_error() != 0:
         raise RuntimeError("kernel wait-limit flag raised during warm-up")
 
-    # The timed work runs as CUDA-graph replays: one step = the six calls, each
-    # preceded by an L2 flush.  A second graph holds the same six flushes and
+    # The timed work runs as CUDA-graph replays: one step = the 14 calls, each
+    # preceded by an L2 flush.  A second graph holds the same flushes and
     # nothing else; its time is subtracted, so the reported time is the qr
     # kernels' device time with launch latency overlapped as in any stream of
-    # work (eager per-call events, reported beside it, also count the ~4 us
-    # launch gap an empty kernel shows between two events).
-    cap_stream = torch.cuda.Stream(device=dev)
-
-    def capture(fn):
-        g = torch.cuda.CUDAGraph()
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=cap_stream):
-            fn()
-        torch.cuda.synchronize()
-        return g
-
-    def replay_time(g, reps):
-        s = torch.cuda.current_stream()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s)
-        for _ in range(reps):
-            g.replay()
-        b.record(s)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) * 1e-3
-
-    flush_graphs = {}
-
-    def per_call_seconds(fn, reps):
-        """Device time of fn per call: [flush, fn] x reps minus [flush] x reps."""
-        fn()  # eager first call: any one-time set-up happens outside capture
-        torch.cuda.synchronize()
-        g1 = capture(lambda: [(flush(), fn()) for _ in range(reps)])
-        if reps not in flush_graphs:
-            flush_graphs[reps] = capture(lambda: [flush() for _ in range(reps)])
-        g0 = flush_graphs[reps]
-        for g in (g1, g0):
-            g.replay()
-        t1 = replay_time(g1, 2) / 2
-        t0 = replay_time(g0, 2) / 2
-        del g1
-        return max((t1 - t0) / reps, 1e-9)
-
-    step_graph = capture(lambda: [(flush(), call(fmt, st)) for fmt, st in STEP_CALLS])
-    flush_graph = capture(lambda: [flush() for _ in STEP_CALLS])
+    # work.
+    step_graph = timer.capture(lambda: [(flush(), call(fmt, st)) for fmt, st in STEP_CALLS])
+    flush_graph = timer.capture(lambda: [flush() for _ in STEP_CALLS])
     for _ in range(args.warmup):
         step_graph.replay()
         flush_graph.replay()
@@ -368,28 +412,29 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.2)
     wall0 = time.perf_counter()
-    t_steps = replay_time(step_graph, K)          # K timed steps (synchronised on both sides)
+    t_steps = timer.replay_time(step_graph, K)          # K timed steps (synchronised on both sides)
     wall = time.perf_counter() - wall0
     dist_barrier()
     clocks = sampler.stop()
-    t_flush = replay_time(flush_graph, K)         # the same flushes alone
+    t_flush = timer.replay_time(flush_graph, K)         # the same flushes alone
     if qr.qr_device_error() != 0:
         raise RuntimeError("kernel wait-limit flag raised in the timed region")
     my_total = t_steps - t_flush
     max_total = dist_max(my_total, dev)
     step_bytes = sum(n * 2 for _ in STEP_CALLS)
     value = aggregate(K * step_bytes, max_total, world)
+    del step_graph, flush_graph
 
     # per-call device times (graphs) and eager event times, for the breakdown
     peak, peak_kind = read_peaks()
     per_format = {}
-    q_bytes = q_time = 0.0
+    q2_bytes = q2_time = all_bytes = all_time = 0.0
     stream = torch.cuda.current_stream()
     for fmt, st in STEP_CALLS:
         b = bytes_alg(W, n, fmt, st, st == 2)
-        t = per_call_seconds(lambda: call(fmt, st), args.graph_reps)
+        t = timer.per_call_seconds(lambda: call(fmt, st), args.graph_reps)
         eager = []
-        for it in range(args.warmup + args.sweep_iters):
+        for it in range(args.warmup + args.eager_iters):
             flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -403,33 +448,65 @@ def run_ours(args):
             "us": round(t * 1e6, 2), "us_eager_events": round(te * 1e6, 2),
             "algbw_GBps": round(n * 2 / t / 1e9, 1), "hbm_GBps": round(b / t / 1e9, 1),
             "frac_of_measured_peak": round(b / t / 1e9 / peak, 3)}
-        if fmt != FP:
-            q_bytes += b
-            q_time += t
-    achieved = q_bytes / q_time / 1e9
+        all_bytes += b
+        all_time += t
+        if fmt != FP and st == 2:
+            q2_bytes += b
+            q2_time += t
+    achieved = q2_bytes / q2_time / 1e9
+    n_q2 = sum(1 for f, st in STEP_CALLS if f != FP and st == 2)
+
+    # ---------------- read-only and write-only streaming rates (torch) ----------------
+    # The measured copy peak moves reads and writes 1:1; the two-stage
+    # allreduce reads W streams and writes about 1.1.  So beside it: the rate
+    # of a pure read (torch's full sum of a 1 GiB fp16 tensor) and of a pure
+    # write (torch's fill_ of 1 GiB), timed exactly like the qr calls, and the
+    # rate they imply for the kernel's mix when its reads and writes take
+    # their own times one after the other: (R + Wb) / (R / read + Wb / write).
+    big = torch.empty(W * n, dtype=torch.float16, device=dev)
+    big.normal_()
+    t_read = timer.per_call_seconds(lambda: big.sum(), args.graph_reps)
+    t_write = timer.per_call_seconds(lambda: big.fill_(1.0), args.graph_reps)
+    bw_read, bw_write = big.numel() * 2 / t_read / 1e9, big.numel() * 2 / t_write / 1e9
+    q2_read = W * n * 2.0
+    q2_written = q2_bytes / n_q2 - q2_read
+    mix_peak = (q2_read + q2_written) / (q2_read / bw_read + q2_written / bw_write)
+    stream_rates = {"read_GBps": round(bw_read, 1), "write_GBps": round(bw_write, 1),
+                    "mix_peak_GBps": round(mix_peak, 1),
+                    "two_stage_quantized_frac_of_mix_peak": round(achieved / mix_peak, 4),
+                    "how": f"read: torch sum of a {big.numel() * 2 >> 20} MiB fp16 tensor; write: torch fill_ of it; "
+                           "each timed like the qr calls; mix_peak = (R + Wb) / (R / read + Wb / write) for the "
+                           "two-stage quantized calls' average read R and written Wb bytes"}
+    del big
+    torch.cuda.empty_cache()
 
     # ---------------- deviation from the exact sum, per format (rank 0) ----------------
     errors = {}
     if rank == 0 and not args.no_extras:
+        idx = sample_block_elems(n, 1 << 15, 5)
+        sub = [h[idx] for h in host]
         for fmt, st in STEP_CALLS:
             call(fmt, st)
             torch.cuda.synchronize()
-            errors[step_name(fmt, st)] = error_vs_exact(host, out.cpu().numpy().view(np.uint16), wl.dtype,
-                                                         fmt, st)
-    traffic = recorded_traffic(os.path.join(ROOT, "quantized_allreduce_codec_gb300", "csrc",
-                                            "qr_device.cuh"))
-    roofline = {"kernel": "qr_pipeline_kernel (fused two-stage, quantized formats FP8/Q8/Q6/Q4, fp16, W=2)",
+            got = out.cpu().numpy().view(np.uint16)[idx]
+            errors[step_name(fmt, st)] = error_vs_exact(sub, got, wl.dtype, fmt, st)
+        errors["sample"] = f"{idx.size // 32} random blocks ({idx.size} elements) of the message"
+    traffic = recorded_traffic(os.path.join(ROOT, "quantized_allreduce_codec_gb300", "csrc", "qr_device.cuh"))
+    roofline = {"kernel": f"qr_pipeline_kernel, fused two-stage, quantized formats (FP8, Q8, Q6, Q4, Q8A, Q4A), "
+                          f"fp16, W={W}: {n_q2} launches per step",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                 else "fallback 6.8 TB/s",
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "frac_of_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": (float(traffic["bytes_per_launch"]) if traffic else None),
-                "algorithmic_bytes_per_launch": round(q_bytes / 4),
-                "traffic_note": (traffic.get("note") if traffic else
-                                 "no ncu capture of the current kernel source"),
+                "algorithmic_bytes_per_launch": round(q2_bytes / n_q2),
+                "traffic_note": (traffic.get("note") if traffic else "no ncu capture of the current kernel source"),
                 "timing": f"per-call device time from CUDA-graph replays ({args.graph_reps} calls, "
-                          "flush-only graph subtracted)"}
+                          "flush-only graph subtracted)",
+                "step_achieved_all_14_launches": round(all_bytes / all_time / 1e9, 1),
+                "step_frac_all_14_launches": round(all_bytes / all_time / 1e9 / peak, 4),
+                "stream_rates": stream_rates}
 
     # ---------------- end to end through the C ABI, host buffers ----------------
     # qr_allreduce_host: page-locked host inputs in, the output back to host
@@ -441,7 +518,6 @@ def run_ours(args):
     pin_out = torch.empty(n, dtype=torch.int16).pin_memory()
     chunk = qr.DEFAULT_HOST_CHUNK
     workspace = qr.host_workspace(W, FP, chunk, device=dev)  # FP's payload is the largest
-    stream = torch.cuda.current_stream()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for warm in (True, False):
         torch.cuda.synchronize()
@@ -458,94 +534,100 @@ def run_ours(args):
            "h2d_bytes_per_step": sum(W * n * 2 for _ in STEP_CALLS),
            "d2h_bytes_per_step": sum(n * 2 for _ in STEP_CALLS), "steps": Ke,
            "note": "qr_allreduce_host on page-locked host buffers: every call copies its W inputs in and "
-                   f"its output back, in chunks of {chunk} elements whose copies overlap the kernels (the stage-2 payload stays on "
-                   "the device)"}
+                   f"its output back, in chunks of {chunk} elements whose copies overlap the kernels (the "
+                   "stage-2 payload stays on the device)"}
     del pin_in, pin_out, workspace
 
-    # ---------------- size sweep (tp2 table sizes, then 128 MiB) ----------------
-    sweep = {}
+    # ---------------- the headline workload through the staged path ----------------
+    extra = {}
     if not args.no_extras:
-        default_limit = qr.qr_direct_limit()
+        st1 = torch.empty(qr.qr_stage1_bytes(W, Q8, n), dtype=torch.uint8, device=dev)
+        res = {}
+        for fmt in (Q8, Q4):
+            t = timer.per_call_seconds(lambda: qr.qr_allreduce_staged(W, wl.dtype, fmt, ins, n, out, wires[fmt],
+                                                                      st1), args.sweep_reps)
+            ba = bytes_alg_staged(W, n, fmt)
+            res[f"{FORMAT_NAMES[fmt]}-2stage-staged"] = {
+                "us": round(t * 1e6, 1), "fused_us": per_format[step_name(fmt, 2)]["us"],
+                "algbw_GBps": round(n * 2 / t / 1e9, 1), "hbm_GBps": round(ba / t / 1e9, 1),
+                "hbm_frac": round(ba / t / 1e9 / peak, 3)}
+        extra[wl.name + " staged"] = res
+        del st1
+    del ins, out, wires
+    torch.cuda.empty_cache()
+
+    # ---------------- tp2 size sweep (the timing table's sizes, then 128 MiB) ----------------
+    sweep, codec, staged = {}, {}, {}
+    if not args.no_extras:
+        tp2 = sweep_workload(TP2_BYTES)
+        tp2_host = workload_inputs(tp2)
+        t_ins = [torch.from_numpy(x.view(np.int16)).to(dev) for x in tp2_host]
+        t_out = torch.empty(tp2.n, dtype=torch.int16, device=dev)
+        t_wires = {f: torch.empty(encoded_bytes(f, tp2.n), dtype=torch.uint8, device=dev) for f, _ in TP2_CALLS}
 
         def sweep_point(nn, sub, o, wdict):
             row = {}
-            # both kernels are timed at every size (the default routing picks one)
-            paths = [("default", default_limit), ("direct", (1 << 64) - 1), ("pipeline", 0)]
-            for fmt, st in STEP_CALLS:
-                entry = {}
-                for pname, limit in paths:
-                    qr.qr_set_direct_limit(limit)
-                    t = per_call_seconds(
-                        lambda: qr.qr_allreduce_emulated(W, wl.dtype, fmt, st, sub, nn, o,
-                                                         wdict[fmt] if st == 2 else None, None),
-                        args.sweep_reps)
-                    if pname == "default":
-                        entry.update({"us": round(t * 1e6, 2),
-                                      "hbm_frac": round(bytes_alg(W, nn, fmt, st, st == 2) / t / 1e9 / peak, 3)})
-                    else:
-                        entry[f"us_{pname}"] = round(t * 1e6, 2)
-                qr.qr_set_direct_limit(default_limit)
-                row[step_name(fmt, st)] = entry
+            for fmt, st in TP2_CALLS:
+                t = timer.per_call_seconds(
+                    lambda: qr.qr_allreduce_emulated(2, F16, fmt, st, sub, nn, o, wdict[fmt] if st == 2 else None,
+                                                     None), args.sweep_reps)
+                row[step_name(fmt, st)] = {"us": round(t * 1e6, 2),
+                                           "hbm_frac": round(bytes_alg(2, nn, fmt, st, st == 2) / t / 1e9 / peak, 3)}
             return row
 
         for size in sweep_sizes_bytes():
             nn = size // 2
-            sweep[str(size)] = sweep_point(nn, [t[:nn] for t in ins], out, wires)
-        # one point past the tp2 table: 128 MiB per rank, its own buffers
+            sweep[str(size)] = sweep_point(nn, [t[:nn] for t in t_ins], t_out, t_wires)
         big = sweep_workload(128 << 20)
-        big_ins = [torch.from_numpy(x.view(np.int16)).to(dev) for x in big.inputs()]
+        big_ins = [torch.from_numpy(x.view(np.int16)).to(dev) for x in workload_inputs(big)]
         big_out = torch.empty(big.n, dtype=torch.int16, device=dev)
-        big_wires = {f: torch.empty(encoded_bytes(f, big.n), dtype=torch.uint8, device=dev) for f, _ in STEP_CALLS}
+        big_wires = {f: torch.empty(encoded_bytes(f, big.n), dtype=torch.uint8, device=dev) for f, _ in TP2_CALLS}
         sweep[str(128 << 20)] = sweep_point(big.n, big_ins, big_out, big_wires)
         del big_ins, big_out, big_wires
         torch.cuda.empty_cache()
 
-    # ---------------- the codec on its own (qr_quantize / qr_dequantize) ----------------
-    codec = {}
-    if not args.no_extras:
-        src = ins[0]
+        # ---------------- the codec on its own (qr_quantize / qr_dequantize) ----------------
+        src = t_ins[0]
+        nn = tp2.n
         for fmt in (FP8, Q8, Q6, Q4, Q8A, Q4A):
-            enc = torch.empty(encoded_bytes(fmt, n), dtype=torch.uint8, device=dev)
-            qr.qr_quantize(wl.dtype, fmt, src, n, enc)
+            enc = torch.empty(encoded_bytes(fmt, nn), dtype=torch.uint8, device=dev)
+            qr.qr_quantize(F16, fmt, src, nn, enc)
             row = {}
-            for name, fn in (("quantize", lambda: qr.qr_quantize(wl.dtype, fmt, src, n, enc)),
-                             ("dequantize", lambda: qr.qr_dequantize(wl.dtype, fmt, enc, n, out))):
-                t = per_call_seconds(fn, args.sweep_reps)
-                ba = n * 2 + encoded_bytes(fmt, n)
+            for name, fn in (("quantize", lambda: qr.qr_quantize(F16, fmt, src, nn, enc)),
+                             ("dequantize", lambda: qr.qr_dequantize(F16, fmt, enc, nn, t_out))):
+                t = timer.per_call_seconds(fn, args.sweep_reps)
+                ba = nn * 2 + encoded_bytes(fmt, nn)
                 row[name] = {"us": round(t * 1e6, 2), "hbm_GBps": round(ba / t / 1e9, 1),
                              "hbm_frac": round(ba / t / 1e9 / peak, 3)}
             codec[FORMAT_NAMES[fmt]] = row
             del enc
 
-    # ---------------- staged two-stage path (stage-1 exchange materialised) ----------------
-    staged = {}
-    if not args.no_extras:
-        st1 = torch.empty(max(qr.qr_stage1_bytes(W, f, n) for f in (FP8, Q8, Q6, Q4)), dtype=torch.uint8,
+        # ---------------- staged two-stage path, tp2 64 MiB ----------------
+        st1 = torch.empty(max(qr.qr_stage1_bytes(2, f, nn) for f in (FP8, Q8, Q6, Q4)), dtype=torch.uint8,
                           device=dev)
         for fmt in (FP8, Q8, Q6, Q4):
-            t = per_call_seconds(lambda: qr.qr_allreduce_staged(W, wl.dtype, fmt, ins, n, out, wires[fmt], st1),
-                                 args.sweep_reps)
-            ba = bytes_alg_staged(W, n, fmt)
-            staged[FORMAT_NAMES[fmt]] = {"us": round(t * 1e6, 2),
-                                         "fused_us": per_format[step_name(fmt, 2)]["us"],
+            t_fused = timer.per_call_seconds(
+                lambda: qr.qr_allreduce_emulated(2, F16, fmt, 2, t_ins, nn, t_out, t_wires[fmt]), args.sweep_reps)
+            t = timer.per_call_seconds(lambda: qr.qr_allreduce_staged(2, F16, fmt, t_ins, nn, t_out, t_wires[fmt],
+                                                                      st1), args.sweep_reps)
+            ba = bytes_alg_staged(2, nn, fmt)
+            staged[FORMAT_NAMES[fmt]] = {"us": round(t * 1e6, 2), "fused_us": round(t_fused * 1e6, 2),
                                          "hbm_GBps": round(ba / t / 1e9, 1),
                                          "hbm_frac": round(ba / t / 1e9 / peak, 3)}
-        del st1
-
-    # ---------------- the other workloads ----------------
-    extra = {}
-    if not args.no_extras:
-        del ins
+        del st1, t_ins, t_out, t_wires
         torch.cuda.empty_cache()
-        for key in (3, 4, 5):
+
+        # ---------------- the other workloads ----------------
+        for key in (3, 4):
             w = workloads()[key]
-            dins = [torch.from_numpy(w.rank_bits(r).view(np.int16)).to(dev) for r in range(w.W)]
+            host_w = workload_inputs(w)
+            dins = [torch.from_numpy(x.view(np.int16)).to(dev) for x in host_w]
             o = torch.empty(w.n, dtype=torch.int16, device=dev)
             res = {}
             for fmt in w.formats:
                 wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
                 for st in w.stages:
-                    t = per_call_seconds(
+                    t = timer.per_call_seconds(
                         lambda: qr.qr_allreduce_emulated(w.W, w.dtype, fmt, st, dins, w.n, o,
                                                          wire if st == 2 else None, None),
                         args.sweep_reps)
@@ -553,44 +635,26 @@ def run_ours(args):
                     res[step_name(fmt, st)] = {"us": round(t * 1e6, 1),
                                                "algbw_GBps": round(w.n * 2 / t / 1e9, 1),
                                                "hbm_GBps": round(ba / t / 1e9, 1),
-                                               "hbm_frac": round(ba / t / 1e9 / peak, 3)}
+                                               "hbm_frac": round(ba / t / 1e9 / peak, 3),
+                                               "frac_of_nominal_8TBps": round(ba / t / 1e9 / NOMINAL_HBM_GBS, 3)}
                 del wire
-            if key in (3, 4):
-                # the bf16 -> fp16 cast option against native bf16: speed, and
-                # error against the exact sum on 4096 sampled blocks
-                host_w = [w.rank_bits(r) for r in range(w.W)]
-                rng = np.random.default_rng(key)
-                blocks = np.sort(rng.choice(w.n // 32, 4096, replace=False))
-                idx = (blocks[:, None] * 32 + np.arange(32)[None, :]).reshape(-1)
-                exact = sum(from_bits(h[idx], BF16).astype(np.float64) for h in host_w)
-                for fmt in w.formats:
-                    wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
-                    row = {}
-                    for tag, dt in (("native_bf16", BF16), ("cast_via_fp16", 2)):
-                        t = per_call_seconds(
-                            lambda: qr.qr_allreduce_emulated(w.W, dt, fmt, 2, dins, w.n, o, wire, None),
-                            args.sweep_reps)
-                        got = from_bits(o.cpu().numpy().view(np.uint16)[idx], BF16).astype(np.float64)
-                        err = np.abs(got - exact)
-                        row[tag] = {"us": round(t * 1e6, 1), "max_abs_err": float(err.max()),
-                                    "mean_abs_err": float(err.mean()),
-                                    "inf_outputs": int(np.isinf(got).sum())}
-                    res[f"{FORMAT_NAMES[fmt]}-2stage-cast-option"] = row
-                    del wire
-            if key == 5:
-                st1 = torch.empty(qr.qr_stage1_bytes(w.W, Q8, w.n), dtype=torch.uint8, device=dev)
-                for fmt in (Q8, Q4):
-                    wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
-                    t = per_call_seconds(
-                        lambda: qr.qr_allreduce_staged(w.W, w.dtype, fmt, dins, w.n, o, wire, st1),
+            # the bf16 -> fp16 cast option against native bf16: speed, and
+            # error against the exact sum on 4096 sampled blocks
+            idx = sample_block_elems(w.n, 4096, key)
+            exact = sum(from_bits(h[idx], BF16).astype(np.float64) for h in host_w)
+            for fmt in w.formats:
+                wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
+                row = {}
+                for tag, dt in (("native_bf16", BF16), ("cast_via_fp16", 2)):
+                    t = timer.per_call_seconds(
+                        lambda: qr.qr_allreduce_emulated(w.W, dt, fmt, 2, dins, w.n, o, wire, None),
                         args.sweep_reps)
-                    ba = bytes_alg_staged(w.W, w.n, fmt)
-                    res[f"{FORMAT_NAMES[fmt]}-2stage-staged"] = {"us": round(t * 1e6, 1),
-                                                                 "algbw_GBps": round(w.n * 2 / t / 1e9, 1),
-                                                                 "hbm_GBps": round(ba / t / 1e9, 1),
-                                                                 "hbm_frac": round(ba / t / 1e9 / peak, 3)}
-                    del wire
-                del st1
+                    got = from_bits(o.cpu().numpy().view(np.uint16)[idx], BF16).astype(np.float64)
+                    err = np.abs(got - exact)
+                    row[tag] = {"us": round(t * 1e6, 1), "max_abs_err": float(err.max()),
+                                "mean_abs_err": float(err.mean()), "inf_outputs": int(np.isinf(got).sum())}
+                res[f"{FORMAT_NAMES[fmt]}-2stage-cast-option"] = row
+                del wire
             extra[w.name] = res
             del dins, o
             torch.cuda.empty_cache()
@@ -608,18 +672,11 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(max_total / K * 1e3, 4),
-            "timing": "K replays of a CUDA graph holding one step (six [L2 flush, qr call] pairs), "
+            "timing": f"K replays of a CUDA graph holding one step ({len(STEP_CALLS)} [L2 flush, qr call] pairs), "
                       "timed with CUDA events, minus K replays of the same graph without the qr calls",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": "tp2 table, largest size: W=2 emulated ranks, fp16, 64 MiB "
-                                   "(33554432 elements) per rank, N(0,1) seed 2000+r; one step = "
-                                   "FP 1-stage, FP 2-stage, FP8, Q8, Q6, Q4 2-stage (payload written)",
-                       "W": W, "per_rank_bytes": n * 2, "calls_per_step": len(STEP_CALLS),
-                       "l2": f"flushed before every timed call, outside the timed events: a "
-                             f"{flush_buf.numel() * 4 >> 20} MiB write, then a {clean_buf.numel() * 4 >> 20} MiB "
-                             "read of a second buffer (no dirty lines left in L2)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, W ranks emulated in HBM"},
+            "config": headline_config(wl, world),
             "roofline": roofline, "per_format": per_format, "error_vs_exact_sum": errors,
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": K * len(STEP_CALLS),
@@ -691,7 +748,7 @@ def host_threads() -> int:
 
 def cpu_baseline(host, dtype, seconds: float) -> dict:
     """The oracle on a prefix of the bench workload sized to about `seconds`
-    of wall time over the step's six calls: on every host core (block runs
+    of wall time over the step's calls: on every host core (block runs
     in parallel threads), and on one core for comparison."""
     import oracle
     oracle.build()
@@ -727,9 +784,10 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    wl = sweep_workload(BENCH_BYTES)
-    m = args.ref_elems
-    host = [wl.rank_bits(r)[:m] for r in range(wl.W)]
+    wl = workloads()[HEADLINE]
+    m = min(args.ref_elems, wl.n)
+    m -= m % 32
+    host = [x[:m].copy() for x in workload_inputs(wl)]
     T = host_threads()
     for _ in range(args.warmup):
         oracle_step(wl.dtype, host, T)
@@ -738,24 +796,101 @@ def run_reference(args):
         oracle_step(wl.dtype, host, T)
     t = time.perf_counter() - t0
     value = args.steps * len(STEP_CALLS) * m * 2 / t / 1e9
+    sample = (f"each step runs all {len(STEP_CALLS)} calls of the step on the first {m} elements "
+              f"({m * 2 >> 10} KiB, {m // 32} blocks) of each rank's message, split into whole-block runs on "
+              f"{T} host threads; the result is defined block by block, so the rate per rank-message byte "
+              "is that of the whole message")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(t / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "tp2 table, largest size: W=2 emulated ranks, fp16, 64 MiB per rank, "
-                               "N(0,1); one step = FP 1-stage, FP 2-stage, FP8, Q8, Q6, Q4 2-stage; "
-                               f"each step runs the CPU oracle on the first {m} elements of each rank, "
-                               f"split into block runs on {T} host threads",
-                   "W": wl.W, "per_rank_bytes": wl.n * 2},
+        "config": headline_config(wl, world),
         "cpu_baseline": {"kind": "oracle", "cores": T, "value": round(value, 6), "unit": "GB/s",
-                         "sample": f"first {m} elements of each rank's message per call, "
-                                   f"in {T} block runs on {T} threads"},
+                         "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "note": "the reference arm is the repository's CPU oracle (no reference implementation ships "
-                "with the source pages)",
+                "with the source pages), timed on a bounded sample of the same workload: " + sample,
     }
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# kernel-path selection sweep (writes the measurements the routing table is
+# generated from: quantized_allreduce_codec_gb300/select_table.py)
+# ----------------------------------------------------------------------------
+def select_grid_bytes() -> list:
+    """Per-rank message sizes of the selection sweep: powers of two from 4 KiB
+    to 128 MiB, plus the midpoints 1.5 MiB, 3 MiB, ..., 96 MiB where the
+    kernels' times cross."""
+    return sorted([4096 << k for k in range(16)] + [3 << (19 + k) for k in range(7)])
+
+
+def run_select_sweep(args):
+    import torch
+
+    import quantized_allreduce_codec_gb300 as qr
+    from quantized_allreduce_codec_gb300 import build as qr_build
+
+    qr_build.build()
+    qr.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    timer = GpuTimer(dev)
+    grid = select_grid_bytes()
+    maxn = grid[-1] // 2
+    gen = torch.Generator(device=dev)
+    records = []
+    t_start = time.time()
+    for dt in (F16, BF16, 2):
+        for W in (1, 2, 4, 8):
+            gen.manual_seed(7000 + 10 * dt + W)
+            ins = []
+            for _ in range(W):  # N(0,1) with 0.1 % of the elements x50, as the LLM-like workloads
+                x = torch.randn(maxn, device=dev, generator=gen)
+                x[torch.rand(maxn, device=dev, generator=gen) < 0.001] *= 50
+                ins.append(x.to(torch.float16 if dt == F16 else torch.bfloat16).view(torch.int16).contiguous())
+                del x
+            out = torch.empty(maxn, dtype=torch.int16, device=dev)
+            wire = torch.empty(encoded_bytes(FP, maxn), dtype=torch.uint8, device=dev)
+            for mode in (0, 1, 2):
+                if mode == 0 and (W != 1 or dt == 2):
+                    continue
+                for fmt in ALL_FORMATS:
+                    for size in grid:
+                        n = size // 2
+                        sub = [x[:n] for x in ins]
+                        if mode == 0:
+                            fn = lambda: qr.qr_quantize(dt, fmt, sub[0], n, wire)  # noqa: E731
+                        else:
+                            fn = lambda: qr.qr_allreduce_emulated(W, dt, fmt, mode, sub, n, out,  # noqa: E731
+                                                                  wire if mode == 2 else None)
+                        reps = 20 if size <= (1 << 20) else 10 if size <= (16 << 20) else 5
+                        rec = {"dt": dt, "mode": mode, "W": W, "fmt": fmt, "n": n}
+                        for path, limit in (("direct", qr.MAX_ELEMS), ("pipeline", 0)):
+                            qr.qr_set_direct_limit(limit)
+                            try:
+                                rec[f"us_{path}"] = round(timer.per_call_seconds(fn, reps) * 1e6, 3)
+                            finally:
+                                qr.qr_set_direct_limit(qr.DIRECT_LIMIT_TABLE)
+                        records.append(rec)
+            del ins, out, wire
+            torch.cuda.empty_cache()
+            print(f"select sweep: dtype {dt} W {W} done ({time.time() - t_start:.0f} s)", file=sys.stderr, flush=True)
+    if qr.qr_device_error() != 0:
+        raise RuntimeError("kernel wait-limit flag raised in the selection sweep")
+    props = torch.cuda.get_device_properties(dev)
+    doc = {"device": props.name, "sms": props.multi_processor_count,
+           "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()),
+           "how": "per call shape (dtype, mode 0 = qr_quantize / 1 = one-stage / 2 = two-stage, W, format) and "
+                  "per-rank size n (elements), the device time per call of the direct and of the pipeline "
+                  "kernel (forced with qr_set_direct_limit), each from CUDA-graph replays of [L2 flush, call] "
+                  "pairs minus the flushes alone, as in bench.py; inputs N(0,1) with 0.1 % x50 outliers",
+           "grid_bytes": grid, "records": records}
+    with open(args.select_sweep, "w") as f:
+        json.dump(doc, f)
+    print(json.dumps({"select_sweep": args.select_sweep, "records": len(records),
+                      "seconds": round(time.time() - t_start, 1)}), flush=True)
 
 
 def main(argv=None):
@@ -765,17 +900,22 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--sweep-iters", type=int, default=20)
-    ap.add_argument("--graph-reps", type=int, default=50, help="calls per graph for per-call times")
+    ap.add_argument("--eager-iters", type=int, default=10)
+    ap.add_argument("--graph-reps", type=int, default=20, help="calls per graph for per-call times")
     ap.add_argument("--sweep-reps", type=int, default=10, help="calls per graph in the sweep/extras")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ref-elems", type=int, default=1 << 18)
+    ap.add_argument("--ref-elems", type=int, default=1 << 20)
     ap.add_argument("--no-extras", action="store_true", help="skip the size sweep and other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--select-sweep", metavar="OUT.json",
+                    help="instead of the bench: time both kernel paths for every call shape over a size grid "
+                         "and write the measurements (the input of select_table.py)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.select_sweep:
+        run_select_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -256,15 +256,32 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages,
                             size_t workspace_bytes, size_t chunk_elems,
                             void *stream);
 
-/* Messages of at most qr_direct_limit() elements per rank are processed by a
- * single-pass kernel with one memory round trip (lowest latency); longer ones
- * by the persistent bulk-copy pipeline (highest bandwidth).  Both compute
- * identical bits.  The default limit is 4194304 elements (8 MiB of fp16);
- * qr_set_direct_limit changes it for the whole process (0: always the
- * pipeline; SIZE_MAX: always the direct kernel).  Host only, no CUDA call;
- * applies to qr_quantize and qr_allreduce_emulated calls made afterwards. */
+/* Kernel-path selection.  Every qr_quantize and qr_allreduce_emulated call is
+ * served by one of two kernels that compute identical bits: a single-pass
+ * kernel with one memory round trip (lowest latency) or the persistent
+ * bulk-copy pipeline (highest bandwidth).  Messages of at most `limit`
+ * elements per rank take the single-pass kernel.  By default the limit comes
+ * from a table measured on GB300 per call shape -- dtype, stage mode
+ * (encode-only, one-stage, two-stage), W and format -- the counterpart, for
+ * this data path, of the per-(dtype, world size) size thresholds _QR_MIN_SIZE
+ * on the vLLM quick_all_reduce page and of the size rule in vLLM PR #18473's
+ * description (the table's source: csrc/qr_select_table.h, generated by
+ * select_table.py from the committed sweep).
+ *
+ * qr_set_direct_limit(n) overrides the table for EVERY call shape in the
+ * whole process (n = 0: always the pipeline; n >= QR_MAX_ELEMS: always the
+ * single-pass kernel) until qr_set_direct_limit(QR_DIRECT_LIMIT_TABLE)
+ * restores the table.  It is process-global state: a caller in another thread
+ * is rerouted too (results stay bit-identical; only timing changes).
+ * qr_direct_limit() returns the override, or QR_DIRECT_LIMIT_TABLE when the
+ * table routes.  qr_selected_direct_limit returns the limit that a call of
+ * the given shape uses now (stages 0: qr_quantize, W ignored; 1 or 2: the
+ * allreduce); 0 for a shape no call can have (0 is also the limit of a shape
+ * that always takes the pipeline).  Host only, no CUDA call; thread-safe. */
+#define QR_DIRECT_LIMIT_TABLE ((size_t)-1)
 size_t qr_direct_limit(void);
 void qr_set_direct_limit(size_t n);
+size_t qr_selected_direct_limit(int W, qr_dtype dt, qr_format fmt, int stages);
 
 /* A short English description of a status code (static storage). */
 const char *qr_status_string(qr_status st);

@@ -27,7 +27,10 @@ LIB_PATH = os.path.join(_HERE, "libqr.so")
 EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
            "qr_status_string", "qr_device_error", "qr_direct_limit", "qr_set_direct_limit",
            "qr_selftest_wait_timeout", "qr_stage1_bytes", "qr_allreduce_staged",
-           "qr_allreduce_staged_noalloc", "qr_host_workspace_bytes", "qr_allreduce_host")
+           "qr_allreduce_staged_noalloc", "qr_host_workspace_bytes", "qr_allreduce_host",
+           "qr_selected_direct_limit")
+MAX_ELEMS = 1 << 36                 # QR_MAX_ELEMS: the largest message (elements)
+DIRECT_LIMIT_TABLE = (1 << 64) - 1  # QR_DIRECT_LIMIT_TABLE: route by the measured table
 DEFAULT_HOST_CHUNK = 1 << 22  # elements per rank per chunk of qr_allreduce_host (8 MiB of fp16)
 
 _lib = None
@@ -70,6 +73,8 @@ def lib():
                 L.qr_direct_limit.argtypes = []
                 L.qr_set_direct_limit.restype = None
                 L.qr_set_direct_limit.argtypes = [sz]
+                L.qr_selected_direct_limit.restype = sz
+                L.qr_selected_direct_limit.argtypes = [i, i, i, i]
                 L.qr_stage1_bytes.restype = sz
                 L.qr_stage1_bytes.argtypes = [i, i, sz]
                 L.qr_allreduce_staged.restype = i
@@ -176,13 +181,22 @@ def qr_device_error(clear: bool = True) -> int:
 
 
 def qr_direct_limit() -> int:
-    """Largest message (elements per rank) handled by the direct kernel."""
+    """The process-wide direct-kernel limit override (elements per rank), or
+    DIRECT_LIMIT_TABLE when the measured per-shape table routes."""
     return int(lib().qr_direct_limit())
 
 
 def qr_set_direct_limit(n: int) -> None:
-    """Set the direct-kernel limit for the process (0: always the pipeline)."""
+    """Override the table for every call shape in the process (0: always the
+    pipeline; MAX_ELEMS: always the direct kernel); DIRECT_LIMIT_TABLE
+    restores the table.  Process-global: other threads are rerouted too."""
     lib().qr_set_direct_limit(n)
+
+
+def qr_selected_direct_limit(W: int, dtype, fmt: int, stages: int) -> int:
+    """The direct-kernel limit a call of this shape uses now (stages 0:
+    qr_quantize; 1, 2: the allreduce)."""
+    return int(lib().qr_selected_direct_limit(W, _dtype_code(dtype), fmt, stages))
 
 
 def qr_selftest_wait_timeout(limit_us: int, stream=None) -> None:

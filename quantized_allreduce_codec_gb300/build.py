@@ -34,7 +34,7 @@ def nvcc() -> str:
 
 def _sources():
     return [os.path.join(CSRC, f) for f in ("qr_api.cu", "qr_kernels.cu", "qr_device.cuh", "qr_launch.h",
-                                             "qr_staged.cuh", "qr_noalloc.cu")] + \
+                                             "qr_staged.cuh", "qr_noalloc.cu", "qr_select_table.h")] + \
         [os.path.join(INCLUDE, "qr.h")]
 
 

@@ -9,6 +9,7 @@
 
 #include "qr.h"
 #include "qr_launch.h"
+#include "qr_select_table.h"
 
 namespace qr {
 
@@ -17,7 +18,6 @@ __device__ unsigned g_qr_error_flags;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr unsigned long long kDefaultDirectLimit = 4ull * 1024 * 1024;  // elements per rank (8 MiB of fp16)
 
 int code_bits(int fmt) {
   switch (fmt) {
@@ -44,8 +44,18 @@ qr_status check_size(size_t n) {
 
 qr_status to_status(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_CUDA; }
 
+// Kernel-path selection: a process-wide override of the measured table
+// (QR_DIRECT_LIMIT_TABLE: none, the table routes).
+std::atomic<unsigned long long> g_direct_override{static_cast<unsigned long long>(QR_DIRECT_LIMIT_TABLE)};
+
+int world_index(int W) { return W == 1 ? 0 : W == 2 ? 1 : W == 4 ? 2 : 3; }
+
 // Messages of at most this many elements per rank take the direct kernel.
-std::atomic<unsigned long long> g_direct_limit{kDefaultDirectLimit};
+unsigned long long direct_limit(int dt, int mode, int W, int fmt) {
+  const unsigned long long o = g_direct_override.load(std::memory_order_relaxed);
+  if (o != static_cast<unsigned long long>(QR_DIRECT_LIMIT_TABLE)) return o;
+  return kDirectLimitTable[dt][mode][world_index(W)][fmt];
+}
 
 cudaError_t dispatch_direct(int fmt, int dt, int mode, const PipeParams& p, cudaStream_t s) {
   switch (fmt) {
@@ -61,7 +71,7 @@ cudaError_t dispatch_direct(int fmt, int dt, int mode, const PipeParams& p, cuda
 }
 
 cudaError_t dispatch_pipeline(int fmt, int dt, int mode, const PipeParams& p, cudaStream_t s) {
-  if (p.n <= g_direct_limit.load(std::memory_order_relaxed)) return dispatch_direct(fmt, dt, mode, p, s);
+  if (p.n <= direct_limit(dt, mode, p.W, fmt)) return dispatch_direct(fmt, dt, mode, p, s);
   switch (fmt) {
     case 0: return launch_pipeline_fmt_0(dt, mode, p, s);
     case 1: return launch_pipeline_fmt_1(dt, mode, p, s);
@@ -515,9 +525,21 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages, const
   return QR_OK;
 }
 
-size_t qr_direct_limit(void) { return static_cast<size_t>(g_direct_limit.load()); }
+size_t qr_direct_limit(void) { return static_cast<size_t>(g_direct_override.load()); }
 
-void qr_set_direct_limit(size_t n) { g_direct_limit.store(static_cast<unsigned long long>(n)); }
+void qr_set_direct_limit(size_t n) { g_direct_override.store(static_cast<unsigned long long>(n)); }
+
+size_t qr_selected_direct_limit(int W, qr_dtype dt, qr_format fmt, int stages) {
+  const int d = static_cast<int>(dt), f = static_cast<int>(fmt);
+  if (!valid_format(f) || stages < 0 || stages > 2) return 0;
+  if (stages == 0) {  // qr_quantize: one rank, fp16 or bf16
+    if (!valid_dtype(d)) return 0;
+    return static_cast<size_t>(direct_limit(d, MODE_ENCODE, 1, f));
+  }
+  if (!valid_dtype(d) && d != DT_BF16_AS_F16) return 0;
+  if (W != 1 && W != 2 && W != 4 && W != 8) return 0;
+  return static_cast<size_t>(direct_limit(d, stages == 1 ? MODE_AR1 : MODE_AR2, W, f));
+}
 
 qr_status qr_selftest_wait_timeout(unsigned int limit_us, void* stream) {
   if (limit_us == 0 || limit_us > 1000000u) return QR_ERR_SIZE;

@@ -85,12 +85,28 @@ cudaError_t launch_pipe_w(const PipeParams& p, cudaStream_t s) {
   return launch_overlapped(kern, grid, kThreads, kSmemBytesOf<M>, s, p);
 }
 
-// Rank count known at compile time where it is fixed or common: 1 for
-// encode-only, 2 for the tp2 case; other W take the general instantiation.
+// The rank count is a compile-time constant in every instantiation (W is
+// one of 1, 2, 4, 8; encode-only runs one rank), except that the two-stage
+// kernel at W = 8 runs the kernel's runtime rank loop (kW8Of = 0): its
+// unrolled eight-rank body plus the requantization measured 1.5-3 % slower
+// on GB300 than the one-rank loop body, while the one-stage kernel at W = 8
+// is 1-2 % faster unrolled.
+template <int F, int D, int M>
+constexpr int kW8Of = M == MODE_AR2 ? 0 : 8;
+
 template <int F, int D, int M>
 cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
-  if (M == MODE_ENCODE) return launch_pipe_w<F, D, M, 1>(p, s);
-  return p.W == 2 ? launch_pipe_w<F, D, M, 2>(p, s) : launch_pipe_w<F, D, M, 0>(p, s);
+  if constexpr (M == MODE_ENCODE) {
+    return launch_pipe_w<F, D, M, 1>(p, s);
+  } else {
+    switch (p.W) {
+      case 1: return launch_pipe_w<F, D, M, 1>(p, s);
+      case 2: return launch_pipe_w<F, D, M, 2>(p, s);
+      case 4: return launch_pipe_w<F, D, M, 4>(p, s);
+      case 8: return launch_pipe_w<F, D, M, kW8Of<F, D, M>>(p, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
 }
 
 template <int F, int D, int M, int WS>
@@ -104,10 +120,19 @@ cudaError_t launch_dir_w(const PipeParams& p, cudaStream_t s) {
   return launch_overlapped(qr_direct_kernel<F, D, M, WS>, grid, kDirectThreads, 0, s, p);
 }
 
-// W = 2 (the tp2 case) has its own instantiation with the rank count known.
 template <int F, int D, int M>
 cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
-  return p.W == 2 ? launch_dir_w<F, D, M, 2>(p, s) : launch_dir_w<F, D, M, 0>(p, s);
+  if constexpr (M == MODE_ENCODE) {
+    return launch_dir_w<F, D, M, 1>(p, s);
+  } else {
+    switch (p.W) {
+      case 1: return launch_dir_w<F, D, M, 1>(p, s);
+      case 2: return launch_dir_w<F, D, M, 2>(p, s);
+      case 4: return launch_dir_w<F, D, M, 4>(p, s);
+      case 8: return launch_dir_w<F, D, M, 8>(p, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
 }
 
 template <int F, int D>

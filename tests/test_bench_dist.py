@@ -6,6 +6,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -72,6 +73,13 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+    # the reference arm describes the very workload the GPU arm times
+    sys.path.insert(0, ROOT)
+    import bench
+    from quantized_allreduce_codec_gb300.inputs import workloads
+    assert line["config"] == bench.headline_config(workloads()[bench.HEADLINE], 1)
+    assert line["config"]["W"] == 8 and line["config"]["per_rank_elems"] == 8192 * 8192
+    assert line["config"]["calls_per_step"] == len(bench.STEP_CALLS) == 14
 
 
 def test_bytes_alg_table():
@@ -81,3 +89,13 @@ def test_bytes_alg_table():
     assert bench.bytes_alg(2, n, 0, 1, False) == 3 * 2 * n
     assert bench.bytes_alg(2, n, 3, 2, True) == 6 * n + n // 32 * 18   # Q4: 16 code bytes + scale
     assert bench.bytes_alg(8, n, 5, 2, True) == 18 * n + n // 32 * 36  # Q8 asym
+
+
+def test_sampled_blocks_are_whole_distinct_and_sorted():
+    sys.path.insert(0, ROOT)
+    import bench
+    idx = bench.sample_block_elems(1 << 16, 100, 3)
+    assert idx.size == 100 * 32
+    blocks = idx.reshape(-1, 32)
+    assert (blocks[:, 0] % 32 == 0).all() and (blocks == blocks[:, :1] + np.arange(32)).all()
+    assert (np.diff(blocks[:, 0]) > 0).all() and blocks.max() < (1 << 16)

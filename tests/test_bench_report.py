@@ -21,7 +21,7 @@ from quantized_allreduce_codec_gb300.inputs import (BF16, F16, FP, Q4, Workload,
 def test_oracle_outputs_meet_the_reported_bounds(oracle_mod, size_bytes):
     wl = sweep_workload(size_bytes)
     host = wl.inputs()
-    for fmt, st in bench.STEP_CALLS:
+    for fmt, st in bench.TP2_CALLS:
         out, _ = oracle_mod.allreduce(wl.dtype, fmt, st, host)
         rep = bench.error_vs_exact(host, out, wl.dtype, fmt, st)
         assert rep["within_bound_fraction"] == 1.0, (fmt, st, rep)

@@ -77,11 +77,44 @@ def test_encoded_bytes_table():
     assert qr.qr_encoded_bytes(9, 1000) == 0
 
 
-def test_direct_limit_knob(L):
+def table_from_header():
+    """kDirectLimitTable[dt][mode][w][fmt] parsed from the generated header."""
+    text = open(os.path.join(ROOT, "quantized_allreduce_codec_gb300", "csrc", "qr_select_table.h")).read()
+    body = text[text.index("kDirectLimitTable"):]
+    vals = [int(v) for v in re.findall(r"(\d+)ull", body)]
+    assert len(vals) == 3 * 3 * 4 * 7
+    return [[[vals[((d * 3 + m) * 4 + w) * 7:((d * 3 + m) * 4 + w) * 7 + 7] for w in range(4)]
+             for m in range(3)] for d in range(3)]
+
+
+def test_selected_limit_follows_the_table(L):
+    tab = table_from_header()
+    assert qr.qr_direct_limit() == qr.DIRECT_LIMIT_TABLE  # the table routes by default
+    for fmt in range(7):
+        for dt in (0, 1):  # qr_quantize: one rank, W ignored
+            assert qr.qr_selected_direct_limit(2, dt, fmt, 0) == tab[dt][0][0][fmt]
+        for dt in (0, 1, 2):
+            for wi, W in enumerate((1, 2, 4, 8)):
+                for stages in (1, 2):
+                    assert qr.qr_selected_direct_limit(W, dt, fmt, stages) == tab[dt][stages][wi][fmt]
+    # shapes no call can have
+    assert qr.qr_selected_direct_limit(2, 2, 1, 0) == 0   # the cast option has no encode-only call
+    assert qr.qr_selected_direct_limit(3, 0, 1, 2) == 0
+    assert qr.qr_selected_direct_limit(2, 0, 7, 2) == 0
+    assert qr.qr_selected_direct_limit(2, 0, 1, 3) == 0
+    assert qr.qr_selected_direct_limit(2, 5, 1, 2) == 0
+
+
+def test_direct_limit_override_is_process_wide_and_reversible(L):
     old = qr.qr_direct_limit()
     try:
         qr.qr_set_direct_limit(12345)
         assert qr.qr_direct_limit() == 12345
+        for W, dt, fmt, st in ((2, 0, 1, 2), (8, 1, 6, 1), (1, 0, 3, 0)):
+            assert qr.qr_selected_direct_limit(W, dt, fmt, st) == 12345
+        qr.qr_set_direct_limit(qr.DIRECT_LIMIT_TABLE)
+        tab = table_from_header()
+        assert qr.qr_selected_direct_limit(8, 1, 6, 1) == tab[1][1][3][6]
     finally:
         qr.qr_set_direct_limit(old)
     assert qr.qr_direct_limit() == old

@@ -53,8 +53,12 @@ def test_two_stage_beyond_2_31_elements(oracle_mod, fmt):
     out = torch.empty(n, dtype=torch.int16, device="cuda")
     wbytes = qr.qr_encoded_bytes(fmt, n)
     wire = torch.empty(wbytes, dtype=torch.uint8, device="cuda")
-    assert n > qr.qr_direct_limit()
-    qr.qr_allreduce_emulated(W, F16, fmt, 2, ins, n, out, wire)  # pipeline kernel
+    limit = qr.qr_direct_limit()
+    try:
+        qr.qr_set_direct_limit(0)  # the pipeline kernel
+        qr.qr_allreduce_emulated(W, F16, fmt, 2, ins, n, out, wire)
+    finally:
+        qr.qr_set_direct_limit(limit)
 
     blocks = boundary_blocks(n, 9200 + fmt)
     sub = [gather_blocks(x, blocks) for x in xs]
@@ -81,7 +85,7 @@ def test_two_stage_beyond_2_31_elements(oracle_mod, fmt):
     wire2 = torch.empty_like(wire)
     limit = qr.qr_direct_limit()
     try:
-        qr.qr_set_direct_limit((1 << 64) - 1)
+        qr.qr_set_direct_limit(qr.MAX_ELEMS)
         qr.qr_allreduce_emulated(W, F16, fmt, 2, ins, n, out2, wire2)
         torch.cuda.synchronize()
     finally:

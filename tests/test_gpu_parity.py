@@ -39,7 +39,7 @@ def path(request):
     """Run the test once through each kernel: the direct (small-message)
     kernel and the bulk-copy pipeline kernel."""
     old = qr.qr_direct_limit()
-    qr.qr_set_direct_limit((1 << 64) - 1 if request.param == "direct" else 0)
+    qr.qr_set_direct_limit(qr.MAX_ELEMS if request.param == "direct" else 0)
     yield request.param
     qr.qr_set_direct_limit(old)
 
@@ -317,9 +317,10 @@ def test_full_compare_64MiB(oracle_mod, fmt, stages):
 
 
 def test_direct_limit_default_and_paths_agree(oracle_mod):
-    """The default limit routes small messages to the direct kernel; both
-    kernels give the same bits on a message that straddles the limit."""
-    assert qr.qr_direct_limit() == 4 * 1024 * 1024
+    """By default the measured table routes every call shape; both kernels
+    give the same bits on a message just past the old fixed 4M-element
+    limit."""
+    assert qr.qr_direct_limit() == qr.DIRECT_LIMIT_TABLE
     rng = np.random.default_rng(7000)
     n = 4 * 1024 * 1024 + 8
     xs = [to_bits(rng.standard_normal(n).astype(np.float32), F16) for _ in range(2)]
@@ -328,7 +329,7 @@ def test_direct_limit_default_and_paths_agree(oracle_mod):
         for fmt in (Q8, Q6, Q4A):
             qr.qr_set_direct_limit(0)
             a, wa = gpu_allreduce(F16, fmt, 2, xs)
-            qr.qr_set_direct_limit((1 << 64) - 1)
+            qr.qr_set_direct_limit(qr.MAX_ELEMS)
             b, wb = gpu_allreduce(F16, fmt, 2, xs)
             assert_bits_equal(a, b, "paths")
             assert np.array_equal(wa, wb)
