@@ -1,7 +1,8 @@
 """The kernel-path table decides which kernel serves a call: a message of
-exactly the selected limit runs the direct kernel and one block-row past it
-the pipeline kernel (seen in the profiler's kernel list), for shapes of every
-mode; the override reroutes every shape and restoring the table undoes it."""
+exactly the selected limit runs the direct kernel and one 8-element step past
+it the pipeline kernel (seen as the kernel node of a captured CUDA graph), for
+shapes of every mode; the override reroutes every shape and restoring the
+table undoes it."""
 import numpy as np
 import pytest
 import torch
@@ -25,15 +26,49 @@ def library():
     assert qr.qr_device_error(clear=True) == 0
 
 
+def _dot_print(g, path):
+    """Write the DOT description of the captured graph g to path: torch's
+    debug_dump, else cudaGraphDebugDotPrint from the process's libcudart on
+    the raw graph handle."""
+    import ctypes
+    import os
+    g.debug_dump(path)
+    if os.path.exists(path):
+        return
+    libs = [ln.split()[-1] for ln in open("/proc/self/maps") if "libcudart.so" in ln]
+    assert libs, "no libcudart loaded"
+    cudart = ctypes.CDLL(libs[0])
+    cudart.cudaGraphDebugDotPrint.argtypes = [ctypes.c_void_p, ctypes.c_char_p, ctypes.c_uint]
+    cudart.cudaGraphDebugDotPrint.restype = ctypes.c_int
+    assert cudart.cudaGraphDebugDotPrint(ctypes.c_void_p(g.raw_cuda_graph()), path.encode(), 1) == 0
+    assert os.path.exists(path)
+
+
 def kernels_launched(fn):
-    """Names of the CUDA kernels fn launches (torch profiler, CUDA activity)."""
-    from torch.profiler import ProfilerActivity, profile
+    """Names of the kernels fn launches, read from the DOT description of a
+    CUDA graph that captures fn (each launch is a kernel node labelled with
+    the kernel's name)."""
+    import os
+    import re
+    import tempfile
+    fn()  # first-call set-up outside the capture
     torch.cuda.synchronize()
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)  # keep the cudaGraph_t after capture
+    except TypeError:
+        g = torch.cuda.CUDAGraph()
+    g.enable_debug_mode()
+    side = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=side):
         fn()
-        torch.cuda.synchronize()
-    names = [e.name for e in prof.events() if "qr_" in e.name]
-    assert names, "the profiler saw no qr kernel (is CUPTI available?)"
+    torch.cuda.synchronize()
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "graph.dot")
+        _dot_print(g, path)
+        text = open(path).read()
+    del g
+    names = sorted(set(re.findall(r"qr_(?:direct|pipeline|decode)_kernel", text)))
+    assert names, "no qr kernel node in the captured graph"
     return names
 
 

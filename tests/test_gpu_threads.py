@@ -1,0 +1,99 @@
+"""First calls from several host threads at once: in a fresh process (empty
+launch caches, error-word address not yet looked up), eight threads -- four
+pairs, each pair on one call shape, so that two threads race on the same
+kernel instantiation's first-call set-up -- call the C ABI at the same moment
+on their own streams.  Every call must return QR_OK and give the bits that
+the same calls give when repeated one after another afterwards, which the
+oracle pins elsewhere."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SCRIPT = r"""
+import ctypes, json, sys, threading
+import torch
+sys.path.insert(0, ROOT)
+import quantized_allreduce_codec_gb300 as qr
+from quantized_allreduce_codec_gb300.inputs import BF16, F16, FP8, Q4, Q4A, Q6, Q8
+
+L = qr.lib()
+torch.cuda.set_device(0)
+g = torch.Generator(device="cuda")
+g.manual_seed(3)
+
+def pipeline_size(W, dt, fmt, stages):
+    # just past the routed direct-kernel limit (the pipeline kernel), capped
+    lim = qr.qr_selected_direct_limit(W, dt, fmt, stages)
+    return min(lim + 8, 1 << 22) if lim < (1 << 22) else 1 << 22
+
+# (kind, W, dtype, fmt, stages, n): allreduce, quantize or staged
+shapes = [("ar", 2, F16, Q8, 2, 40000),
+          ("ar", 4, BF16, Q4A, 2, pipeline_size(4, BF16, Q4A, 2)),
+          ("quant", 1, F16, Q6, 0, pipeline_size(1, F16, Q6, 0)),
+          ("staged", 8, F16, FP8, 2, 3 * 8192 + 40)]
+jobs = []
+for shape in shapes:
+    kind, W, dt, fmt, st, n = shape
+    for _ in range(2):  # two threads per shape: they race on the same caches
+        ins = [torch.randn(n, device="cuda", generator=g).to(torch.float16 if dt == F16 else torch.bfloat16)
+               .view(torch.int16) for _ in range(W)]
+        out = torch.zeros(n, dtype=torch.int16, device="cuda")
+        wire = torch.zeros(qr.qr_encoded_bytes(fmt, n), dtype=torch.uint8, device="cuda")
+        st1 = (torch.zeros(qr.qr_stage1_bytes(W, fmt, n), dtype=torch.uint8, device="cuda")
+               if kind == "staged" else None)
+        jobs.append(dict(shape=shape, ins=ins, out=out, wire=wire, st1=st1, stream=torch.cuda.Stream()))
+torch.cuda.synchronize()
+
+def call(job, stream_handle):
+    kind, W, dt, fmt, st, n = job["shape"]
+    arr = (ctypes.c_void_p * W)(*[x.data_ptr() for x in job["ins"]])
+    if kind == "ar":
+        return L.qr_allreduce_emulated(W, dt, fmt, st, ctypes.cast(arr, ctypes.c_void_p), n,
+                                       job["out"].data_ptr(), job["wire"].data_ptr(), stream_handle)
+    if kind == "quant":
+        return L.qr_quantize(dt, fmt, job["ins"][0].data_ptr(), n, job["wire"].data_ptr(), stream_handle)
+    return L.qr_allreduce_staged(W, dt, fmt, ctypes.cast(arr, ctypes.c_void_p), n, job["out"].data_ptr(),
+                                 job["wire"].data_ptr(), job["st1"].data_ptr(), stream_handle)
+
+status = [None] * len(jobs)
+gate = threading.Barrier(len(jobs))
+def worker(i):
+    torch.cuda.set_device(0)
+    handle = jobs[i]["stream"].cuda_stream
+    gate.wait()  # every thread's first call at the same moment
+    status[i] = call(jobs[i], handle)
+threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(jobs))]
+for t in threads:
+    t.start()
+for t in threads:
+    t.join()
+torch.cuda.synchronize()
+first = [(j["out"].clone(), j["wire"].clone()) for j in jobs]
+same = []
+for i, j in enumerate(jobs):  # the same calls again, one after another
+    j["out"].zero_()
+    j["wire"].zero_()
+    assert call(j, torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    same.append(bool(torch.equal(first[i][0], j["out"]) and torch.equal(first[i][1], j["wire"])))
+print(json.dumps({"status": status, "same": same, "flags": qr.qr_device_error()}))
+"""
+
+
+def test_first_calls_from_eight_threads_in_a_fresh_process():
+    from quantized_allreduce_codec_gb300 import build
+    build.build()
+    r = subprocess.run([sys.executable, "-c", SCRIPT.replace("ROOT", repr(ROOT), 1)], capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["status"] == [0] * 8, res
+    assert all(res["same"]), res
+    assert res["flags"] == 0
