@@ -31,7 +31,7 @@ g.manual_seed(3)
 def pipeline_size(W, dt, fmt, stages):
     # just past the routed direct-kernel limit (the pipeline kernel), capped
     lim = qr.qr_selected_direct_limit(W, dt, fmt, stages)
-    return min(lim + 8, 1 << 22) if lim < (1 << 22) else 1 << 22
+    return min(lim + 8, 1 << 24) if lim < (1 << 24) else 1 << 24
 
 # (kind, W, dtype, fmt, stages, n): allreduce, quantize or staged
 shapes = [("ar", 2, F16, Q8, 2, 40000),
