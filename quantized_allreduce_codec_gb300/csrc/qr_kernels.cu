@@ -109,15 +109,24 @@ cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   }
 }
 
+// The direct kernel at W = 8 gets one CTA per 256 chunks, so each warp makes
+// one pass (eight ranks' loads, the fold, the stores) and new CTAs start as
+// earlier ones retire: on GB300 3-5 % faster from 4 MiB per rank up than a
+// grid of resident CTAs looping over the message.  At W = 2 and 4 the
+// resident grid measured as fast or faster (up to 5 % at 128 MiB) and stays.
 template <int F, int D, int M, int WS>
 cudaError_t launch_dir_w(const PipeParams& p, cudaStream_t s) {
-  static std::atomic<unsigned long long> cap[kMaxDevices];
-  unsigned long long max_grid = 0;
-  cudaError_t e = resident_ctas(qr_direct_kernel<F, D, M, WS>, kDirectThreads, 0, cap, &max_grid);
-  if (e != cudaSuccess) return e;
-  const unsigned long long want = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;
-  const unsigned grid = static_cast<unsigned>(want < max_grid ? want : max_grid);
-  return launch_overlapped(qr_direct_kernel<F, D, M, WS>, grid, kDirectThreads, 0, s, p);
+  const unsigned long long want = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;  // at most 2^25
+  if constexpr (WS == 8) {
+    return launch_overlapped(qr_direct_kernel<F, D, M, WS>, static_cast<unsigned>(want), kDirectThreads, 0, s, p);
+  } else {
+    static std::atomic<unsigned long long> cap[kMaxDevices];
+    unsigned long long max_grid = 0;
+    cudaError_t e = resident_ctas(qr_direct_kernel<F, D, M, WS>, kDirectThreads, 0, cap, &max_grid);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(want < max_grid ? want : max_grid);
+    return launch_overlapped(qr_direct_kernel<F, D, M, WS>, grid, kDirectThreads, 0, s, p);
+  }
 }
 
 template <int F, int D, int M>
@@ -135,32 +144,27 @@ cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
   }
 }
 
+// The decoder gets one CTA per kDecodeThreads x kDecodeUnroll chunks, so each
+// thread makes one pass (its loads issued together, then its stores) and
+// the hardware starts new CTAs as earlier ones retire; on GB300 this was 3-7 %
+// faster than a grid of resident CTAs looping over the message, whose threads
+// drain their loads between iterations.  (At most 2^36 / 8 / 1024 CTAs.)
 template <int F, int D>
 cudaError_t launch_dec(const DecodeParams& p, cudaStream_t s) {
-  static std::atomic<unsigned long long> cap[kMaxDevices];
-  unsigned long long max_grid = 0;
-  cudaError_t e = resident_ctas(qr_decode_kernel<F, D>, kDecodeThreads, 0, cap, &max_grid);
-  if (e != cudaSuccess) return e;
   const unsigned long long per_cta = (unsigned long long)kDecodeThreads * kDecodeUnroll;
-  const unsigned long long want = (p.n / 8 + per_cta - 1) / per_cta;
-  const unsigned grid = static_cast<unsigned>(want < max_grid ? want : max_grid);
-  return launch_overlapped(qr_decode_kernel<F, D>, grid, kDecodeThreads, 0, s, p);
+  const unsigned long long grid = (p.n / 8 + per_cta - 1) / per_cta;
+  return launch_overlapped(qr_decode_kernel<F, D>, static_cast<unsigned>(grid), kDecodeThreads, 0, s, p);
 }
 
+// The staged kernels get one thread per block, one pass each (new CTAs start
+// as earlier ones retire): at W = 2 and 64 MiB per rank 7-8 % faster on GB300
+// than resident CTAs looping over the message, at W = 8 within 1.5 %.
 template <int F, int D, int WS>
 cudaError_t launch_stg_w(const StagedParams& p, const DecodeParams& dp, cudaStream_t s) {
-  static std::atomic<unsigned long long> cap1[kMaxDevices], cap2[kMaxDevices];
-  unsigned long long max1 = 0, max2 = 0;
-  cudaError_t e = resident_ctas(qr_scatter_encode_kernel<F, D, WS>, kStagedThreads, 0, cap1, &max1);
+  const unsigned grid = static_cast<unsigned>((p.nb + kStagedThreads - 1) / kStagedThreads);  // at most 2^23
+  cudaError_t e = launch_overlapped(qr_scatter_encode_kernel<F, D, WS>, grid, kStagedThreads, 0, s, p);
   if (e != cudaSuccess) return e;
-  e = resident_ctas(qr_owner_reduce_kernel<F, D, WS>, kStagedThreads, 0, cap2, &max2);
-  if (e != cudaSuccess) return e;
-  const unsigned long long want = (p.nb + kStagedThreads - 1) / kStagedThreads;
-  e = launch_overlapped(qr_scatter_encode_kernel<F, D, WS>, static_cast<unsigned>(want < max1 ? want : max1),
-                        kStagedThreads, 0, s, p);
-  if (e != cudaSuccess) return e;
-  e = launch_overlapped(qr_owner_reduce_kernel<F, D, WS>, static_cast<unsigned>(want < max2 ? want : max2),
-                        kStagedThreads, 0, s, p);
+  e = launch_overlapped(qr_owner_reduce_kernel<F, D, WS>, grid, kStagedThreads, 0, s, p);
   if (e != cudaSuccess) return e;
   return launch_dec<F, D>(dp, s);
 }
