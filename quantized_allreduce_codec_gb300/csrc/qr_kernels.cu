@@ -129,10 +129,17 @@ cudaError_t launch_dir_w(const PipeParams& p, cudaStream_t s) {
   }
 }
 
+// The direct path's encoder (qr_quantize): one CTA per 256 blocks, one pass.
+template <int F, int D>
+cudaError_t launch_enc(const PipeParams& p, cudaStream_t s) {
+  const unsigned long long grid = (p.nb + kEncodeBlocksPerCta - 1) / kEncodeBlocksPerCta;  // at most 2^23
+  return launch_overlapped(qr_encode_kernel<F, D>, static_cast<unsigned>(grid), kEncodeThreads, 0, s, p);
+}
+
 template <int F, int D, int M>
 cudaError_t launch_dir(const PipeParams& p, cudaStream_t s) {
   if constexpr (M == MODE_ENCODE) {
-    return launch_dir_w<F, D, M, 1>(p, s);
+    return launch_enc<F, D>(p, s);
   } else {
     switch (p.W) {
       case 1: return launch_dir_w<F, D, M, 1>(p, s);

@@ -67,13 +67,15 @@ def kernels_launched(fn):
         _dot_print(g, path)
         text = open(path).read()
     del g
-    names = sorted(set(re.findall(r"qr_(?:direct|pipeline|decode)_kernel", text)))
+    names = sorted(set(re.findall(r"qr_(?:direct|encode|pipeline|decode)_kernel", text)))
     assert names, "no qr kernel node in the captured graph"
     return names
 
 
 def path_of(names):
-    direct = any("qr_direct_kernel" in nm for nm in names)
+    """The path a call took: the direct kernel (qr_encode_kernel for
+    encode-only calls) or the pipeline kernel."""
+    direct = any("qr_direct_kernel" in nm or "qr_encode_kernel" in nm for nm in names)
     pipe = any("qr_pipeline_kernel" in nm for nm in names)
     assert direct != pipe, names
     return "direct" if direct else "pipeline"
