@@ -922,6 +922,69 @@ def run_select_sweep(args):
                       "seconds": round(time.time() - t_start, 1)}), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# small cases for a profiler (ncu): a few launches each, a few GB at most
+# ----------------------------------------------------------------------------
+PROFILE_CASES = ("step16M", "w4-bf16-2048x4096-q4a")
+
+
+def run_profile_case(args):
+    """Launch one small case for a profiler, then exit.
+    step16M[:FMT:STAGES]: the headline step's calls (every format one- and
+      two-stage, or the one named) at 16M elements per rank -- a quarter of
+      the W=8 8192x8192 workload, 256 MiB of inputs, drawn with the same
+      recipe (N(0,1), 0.1 % x50) from torch's generator -- each on the kernel
+      the library routes the full-size call to (forced with the override),
+      each launched twice (the first launch warms up).
+    w4-bf16-2048x4096-q4a: the W=4 bf16 2048x4096 workload's Q4A two-stage
+      call on its own inputs, launched three times."""
+    import torch
+
+    import quantized_allreduce_codec_gb300 as qr
+    from quantized_allreduce_codec_gb300 import build as qr_build
+    qr_build.build()
+    qr.lib()
+    dev = torch.device("cuda", 0)
+    name, *rest = args.profile_case.split(":")
+    done = []
+    if name == "step16M":
+        W, n, full = 8, 16 << 20, workloads()[HEADLINE].n
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        xs = []
+        for _ in range(W):
+            x = torch.randn(n, device=dev, generator=g)
+            x[torch.rand(n, device=dev, generator=g) < 0.001] *= 50
+            xs.append(x.half().view(torch.int16).contiguous())
+            del x
+        out = torch.empty(n, dtype=torch.int16, device=dev)
+        wire = torch.empty(encoded_bytes(FP, n), dtype=torch.uint8, device=dev)
+        calls = [(int(rest[0]), int(rest[1]))] if rest else STEP_CALLS
+        route = {c: served_by(qr, W, F16, c[0], c[1], full) for c in calls}  # before any override
+        try:
+            for fmt, st in calls:
+                qr.qr_set_direct_limit(qr.MAX_ELEMS if route[(fmt, st)] == "qr_direct_kernel" else 0)
+                for _ in range(2):
+                    qr.qr_allreduce_emulated(W, F16, fmt, st, xs, n, out, wire if st == 2 else None)
+                done.append({"call": step_name(fmt, st), "kernel": route[(fmt, st)]})
+        finally:
+            qr.qr_set_direct_limit(qr.DIRECT_LIMIT_TABLE)
+    elif name == "w4-bf16-2048x4096-q4a":
+        w = workloads()[3]
+        xs = [torch.from_numpy(x.view(np.int16)).to(dev) for x in workload_inputs(w)]
+        out = torch.empty(w.n, dtype=torch.int16, device=dev)
+        wire = torch.empty(encoded_bytes(Q4A, w.n), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            qr.qr_allreduce_emulated(w.W, w.dtype, Q4A, 2, xs, w.n, out, wire)
+        done.append({"call": "Q4A-2stage", "kernel": served_by(qr, w.W, w.dtype, Q4A, 2, w.n)})
+    else:
+        raise SystemExit(f"unknown profile case {args.profile_case!r} (one of {PROFILE_CASES})")
+    torch.cuda.synchronize()
+    if qr.qr_device_error() != 0:
+        raise RuntimeError("kernel wait-limit flag raised")
+    print(json.dumps({"profile_case": args.profile_case, "calls": done}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -936,13 +999,17 @@ def main(argv=None):
     ap.add_argument("--ref-elems", type=int, default=1 << 20)
     ap.add_argument("--no-extras", action="store_true", help="skip the size sweep and other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", metavar="NAME",
+                    help=f"instead of the bench: launch one small case for a profiler ({', '.join(PROFILE_CASES)})")
     ap.add_argument("--select-sweep", metavar="OUT.json",
                     help="instead of the bench: time both kernel paths for every call shape over a size grid "
                          "and write the measurements (the input of select_table.py)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.select_sweep:
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.select_sweep:
         run_select_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
