@@ -925,7 +925,7 @@ def run_select_sweep(args):
 # ----------------------------------------------------------------------------
 # small cases for a profiler (ncu): a few launches each, a few GB at most
 # ----------------------------------------------------------------------------
-PROFILE_CASES = ("step16M", "w4-bf16-2048x4096-q4a")
+PROFILE_CASES = ("step16M", "w4-bf16-2048x4096-q4a", "codec-32M:FMT", "staged-w2-32M:FMT", "tp2-64MiB:FMT:STAGES")
 
 
 def run_profile_case(args):
@@ -937,7 +937,14 @@ def run_profile_case(args):
       the library routes the full-size call to (forced with the override),
       each launched twice (the first launch warms up).
     w4-bf16-2048x4096-q4a: the W=4 bf16 2048x4096 workload's Q4A two-stage
-      call on its own inputs, launched three times."""
+      call on its own inputs, launched three times.
+    codec-32M:FMT: qr_quantize then qr_dequantize of a 32M-element fp16
+      N(0,1) message in format FMT, three times each.
+    staged-w2-32M:FMT: qr_allreduce_staged, W=2 fp16 N(0,1), 32M elements
+      per rank, format FMT, three times.
+    tp2-64MiB:FMT:STAGES: the tp2 table's largest size (W=2 fp16 N(0,1), 64
+      MiB per rank, its seeded inputs), one call three times, routed by the
+      library."""
     import torch
 
     import quantized_allreduce_codec_gb300 as qr
@@ -977,6 +984,34 @@ def run_profile_case(args):
         for _ in range(3):
             qr.qr_allreduce_emulated(w.W, w.dtype, Q4A, 2, xs, w.n, out, wire)
         done.append({"call": "Q4A-2stage", "kernel": served_by(qr, w.W, w.dtype, Q4A, 2, w.n)})
+    elif name in ("codec-32M", "staged-w2-32M") and rest:
+        fmt, n = int(rest[0]), 32 << 20
+        g = torch.Generator(device=dev)
+        g.manual_seed(6)
+        xs = [torch.randn(n, device=dev, generator=g).half().view(torch.int16) for _ in range(2)]
+        enc = torch.empty(encoded_bytes(fmt, n), dtype=torch.uint8, device=dev)
+        out = torch.empty(n, dtype=torch.int16, device=dev)
+        if name == "codec-32M":
+            for _ in range(3):
+                qr.qr_quantize(F16, fmt, xs[0], n, enc)
+                qr.qr_dequantize(F16, fmt, enc, n, out)
+            done.append({"call": f"quantize, dequantize {FORMAT_NAMES[fmt]}",
+                         "kernel": served_by(qr, 1, F16, fmt, 0, n) + ", qr_decode_kernel"})
+        else:
+            st1 = torch.empty(qr.qr_stage1_bytes(2, fmt, n), dtype=torch.uint8, device=dev)
+            for _ in range(3):
+                qr.qr_allreduce_staged(2, F16, fmt, xs, n, out, enc, st1)
+            done.append({"call": f"staged {FORMAT_NAMES[fmt]}",
+                         "kernel": "qr_scatter_encode_kernel, qr_owner_reduce_kernel, qr_decode_kernel"})
+    elif name == "tp2-64MiB" and len(rest) == 2:
+        fmt, st = int(rest[0]), int(rest[1])
+        w = sweep_workload(TP2_BYTES)
+        xs = [torch.from_numpy(x.view(np.int16)).to(dev) for x in workload_inputs(w)]
+        out = torch.empty(w.n, dtype=torch.int16, device=dev)
+        wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            qr.qr_allreduce_emulated(2, F16, fmt, st, xs, w.n, out, wire if st == 2 else None)
+        done.append({"call": step_name(fmt, st), "kernel": served_by(qr, 2, F16, fmt, st, w.n)})
     else:
         raise SystemExit(f"unknown profile case {args.profile_case!r} (one of {PROFILE_CASES})")
     torch.cuda.synchronize()
