@@ -277,8 +277,12 @@ def recorded_traffic():
 
 
 def served_by(qr, W: int, dtype: int, fmt: int, stages: int, n: int) -> str:
-    """The kernel that serves a call of this shape (the library's routing)."""
-    return "qr_direct_kernel" if n <= qr.qr_selected_direct_limit(W, dtype, fmt, stages) else "qr_pipeline_kernel"
+    """The kernel that serves a call of this shape (the library's routing;
+    stages 0 = qr_quantize)."""
+    path = qr.qr_kernel_path(W, dtype, fmt, stages, n)
+    if path == qr.PATH_DIRECT:
+        return "qr_encode_kernel" if stages == 0 else "qr_direct_kernel"
+    return "qr_pipeline_kernel"
 
 
 # ----------------------------------------------------------------------------
@@ -896,12 +900,12 @@ def run_select_sweep(args):
                                                                   wire if mode == 2 else None)
                         reps = 20 if size <= (1 << 20) else 10 if size <= (16 << 20) else 5
                         rec = {"dt": dt, "mode": mode, "W": W, "fmt": fmt, "n": n}
-                        for path, limit in (("direct", qr.MAX_ELEMS), ("pipeline", 0)):
-                            qr.qr_set_direct_limit(limit)
-                            try:
-                                rec[f"us_{path}"] = round(timer.per_call_seconds(fn, reps) * 1e6, 3)
-                            finally:
-                                qr.qr_set_direct_limit(qr.DIRECT_LIMIT_TABLE)
+                        paths = [("direct", qr.PATH_DIRECT), ("pipeline", qr.PATH_PIPELINE)]
+                        if W <= 4:  # narrow tiles are built for W <= 4
+                            paths.append(("narrow", qr.PATH_PIPELINE_NARROW))
+                        for name, path in paths:
+                            with qr.forced_kernel_path(path):
+                                rec[f"us_{name}"] = round(timer.per_call_seconds(fn, reps) * 1e6, 3)
                         records.append(rec)
             del ins, out, wire
             torch.cuda.empty_cache()
@@ -912,8 +916,9 @@ def run_select_sweep(args):
     doc = {"device": props.name, "sms": props.multi_processor_count,
            "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime()),
            "how": "per call shape (dtype, mode 0 = qr_quantize / 1 = one-stage / 2 = two-stage, W, format) and "
-                  "per-rank size n (elements), the device time per call of the direct and of the pipeline "
-                  "kernel (forced with qr_set_direct_limit), each from CUDA-graph replays of [L2 flush, call] "
+                  "per-rank size n (elements), the device time per call of the direct kernel, the wide-tile "
+                  "pipeline and (W <= 4) the narrow-tile pipeline, each forced with qr_set_kernel_path, "
+                  "from CUDA-graph replays of [L2 flush, call] "
                   "pairs minus the flushes alone, as in bench.py; inputs N(0,1) with 0.1 % x50 outliers",
            "grid_bytes": grid, "records": records}
     with open(args.select_sweep, "w") as f:
@@ -967,15 +972,11 @@ def run_profile_case(args):
         out = torch.empty(n, dtype=torch.int16, device=dev)
         wire = torch.empty(encoded_bytes(FP, n), dtype=torch.uint8, device=dev)
         calls = [(int(rest[0]), int(rest[1]))] if rest else STEP_CALLS
-        route = {c: served_by(qr, W, F16, c[0], c[1], full) for c in calls}  # before any override
-        try:
-            for fmt, st in calls:
-                qr.qr_set_direct_limit(qr.MAX_ELEMS if route[(fmt, st)] == "qr_direct_kernel" else 0)
+        for fmt, st in calls:
+            with qr.forced_kernel_path(qr.qr_kernel_path(W, F16, fmt, st, full)):
                 for _ in range(2):
                     qr.qr_allreduce_emulated(W, F16, fmt, st, xs, n, out, wire if st == 2 else None)
-                done.append({"call": step_name(fmt, st), "kernel": route[(fmt, st)]})
-        finally:
-            qr.qr_set_direct_limit(qr.DIRECT_LIMIT_TABLE)
+            done.append({"call": step_name(fmt, st), "kernel": served_by(qr, W, F16, fmt, st, full)})
     elif name == "w4-bf16-2048x4096-q4a":
         w = workloads()[3]
         xs = [torch.from_numpy(x.view(np.int16)).to(dev) for x in workload_inputs(w)]

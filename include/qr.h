@@ -103,8 +103,9 @@ typedef enum {
   QR_ERR_OVERLAP = 8, /* an output buffer overlaps an input or another output */
   QR_ERR_CUDA = 9,    /* the CUDA runtime reported an error                   */
   QR_ERR_DEVICE = 10, /* a kernel gave up waiting (see qr_device_error)      */
-  QR_ERR_SCRATCH = 11 /* qr_allreduce_staged_noalloc: the message needs more
-                         stage-1 space than QR_NOALLOC_SCRATCH_BYTES         */
+  QR_ERR_SCRATCH = 11, /* qr_allreduce_staged_noalloc: the message needs more
+                          stage-1 space than QR_NOALLOC_SCRATCH_BYTES        */
+  QR_ERR_PATH = 12     /* qr_set_kernel_path: not one of the qr_path values   */
 } qr_status;
 
 /* Largest n accepted (elements per message): 2^36. */
@@ -257,31 +258,43 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages,
                             void *stream);
 
 /* Kernel-path selection.  Every qr_quantize and qr_allreduce_emulated call is
- * served by one of two kernels that compute identical bits: a single-pass
- * kernel with one memory round trip (lowest latency) or the persistent
- * bulk-copy pipeline (highest bandwidth).  Messages of at most `limit`
- * elements per rank take the single-pass kernel.  By default the limit comes
- * from a table measured on GB300 per call shape -- dtype, stage mode
- * (encode-only, one-stage, two-stage), W and format -- the counterpart, for
- * this data path, of the per-(dtype, world size) size thresholds _QR_MIN_SIZE
- * on the vLLM quick_all_reduce page and of the size rule in vLLM PR #18473's
- * description (the table's source: csrc/qr_select_table.h, generated by
- * select_table.py from the committed sweep).
+ * served by one of three kernels that compute identical bits:
+ *   QR_PATH_DIRECT           a single-pass kernel with one memory round trip
+ *                            (lowest latency);
+ *   QR_PATH_PIPELINE_NARROW  the persistent bulk-copy pipeline with 8 KiB tiles
+ *                            (mid-size messages: a shorter first fill and
+ *                            last round);
+ *   QR_PATH_PIPELINE         the same pipeline with 16 KiB tiles (highest
+ *                            bandwidth on large messages).
+ * By default the path comes from tables measured on GB300 per call shape --
+ * dtype, stage mode (encode-only, one-stage, two-stage), W and format -- as
+ * two size limits: messages of at most the direct limit (elements per rank)
+ * take the direct kernel, those of at most the narrow-tile limit the
+ * narrow-tile pipeline, longer ones the wide-tile pipeline.  This is the
+ * counterpart, for this data path, of the per-(dtype, world size) size
+ * thresholds _QR_MIN_SIZE on the vLLM quick_all_reduce page and of the size
+ * rule in vLLM PR #18473's description (the tables: csrc/qr_select_table.h,
+ * generated by select_table.py from the committed sweep).  The narrow-tile
+ * pipeline is built for W <= 4; a W = 8 call sent there runs wide tiles.
  *
- * qr_set_direct_limit(n) overrides the table for EVERY call shape in the
- * whole process (n = 0: always the pipeline; n >= QR_MAX_ELEMS: always the
- * single-pass kernel) until qr_set_direct_limit(QR_DIRECT_LIMIT_TABLE)
- * restores the table.  It is process-global state: a caller in another thread
- * is rerouted too (results stay bit-identical; only timing changes).
- * qr_direct_limit() returns the override, or QR_DIRECT_LIMIT_TABLE when the
- * table routes.  qr_selected_direct_limit returns the limit that a call of
- * the given shape uses now (stages 0: qr_quantize, W ignored; 1 or 2: the
- * allreduce); 0 for a shape no call can have (0 is also the limit of a shape
- * that always takes the pipeline).  Host only, no CUDA call; thread-safe. */
-#define QR_DIRECT_LIMIT_TABLE ((size_t)-1)
-size_t qr_direct_limit(void);
-void qr_set_direct_limit(size_t n);
-size_t qr_selected_direct_limit(int W, qr_dtype dt, qr_format fmt, int stages);
+ * qr_kernel_path returns the path a call of the given shape and size takes
+ * now (stages 0: qr_quantize, W ignored; 1 or 2: the allreduce), or -1 for a
+ * shape no call can have.  qr_set_kernel_path(path) forces one path for
+ * EVERY call in the whole process until qr_set_kernel_path(QR_PATH_TABLE)
+ * restores the tables (QR_ERR_PATH for any other value; the setting is then
+ * unchanged).  It is process-global state: a caller in another thread is
+ * rerouted too (results stay bit-identical; only timing changes).
+ * qr_forced_kernel_path returns the forced path, or QR_PATH_TABLE.  Host
+ * only, no CUDA call; thread-safe (one atomic word). */
+typedef enum {
+  QR_PATH_TABLE = -1,
+  QR_PATH_DIRECT = 0,
+  QR_PATH_PIPELINE_NARROW = 1,
+  QR_PATH_PIPELINE = 2
+} qr_path;
+int qr_kernel_path(int W, qr_dtype dt, qr_format fmt, int stages, size_t n);
+qr_status qr_set_kernel_path(int path);
+int qr_forced_kernel_path(void);
 
 /* A short English description of a status code (static storage). */
 const char *qr_status_string(qr_status st);

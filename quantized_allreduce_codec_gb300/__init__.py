@@ -20,17 +20,18 @@ FORMATS = {"FP": QR_FP, "Q8": QR_Q8, "Q6": QR_Q6, "Q4": QR_Q4, "FP8": QR_FP8,
            "Q8A": QR_Q8_ASYM, "Q4A": QR_Q4_ASYM}
 STATUS = ["QR_OK", "QR_ERR_NULL", "QR_ERR_DTYPE", "QR_ERR_FORMAT", "QR_ERR_WORLD",
           "QR_ERR_STAGES", "QR_ERR_SIZE", "QR_ERR_ALIGN", "QR_ERR_OVERLAP", "QR_ERR_CUDA",
-          "QR_ERR_DEVICE", "QR_ERR_SCRATCH"]
+          "QR_ERR_DEVICE", "QR_ERR_SCRATCH", "QR_ERR_PATH"]
+# kernel paths (qr_path)
+PATH_TABLE, PATH_DIRECT, PATH_PIPELINE_NARROW, PATH_PIPELINE = -1, 0, 1, 2
+PATH_NAMES = {PATH_DIRECT: "direct", PATH_PIPELINE_NARROW: "pipeline_narrow", PATH_PIPELINE: "pipeline"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqr.so")
 EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
-           "qr_status_string", "qr_device_error", "qr_direct_limit", "qr_set_direct_limit",
-           "qr_selftest_wait_timeout", "qr_stage1_bytes", "qr_allreduce_staged",
-           "qr_allreduce_staged_noalloc", "qr_host_workspace_bytes", "qr_allreduce_host",
-           "qr_selected_direct_limit")
-MAX_ELEMS = 1 << 36                 # QR_MAX_ELEMS: the largest message (elements)
-DIRECT_LIMIT_TABLE = (1 << 64) - 1  # QR_DIRECT_LIMIT_TABLE: route by the measured table
+           "qr_status_string", "qr_device_error", "qr_kernel_path", "qr_set_kernel_path",
+           "qr_forced_kernel_path", "qr_selftest_wait_timeout", "qr_stage1_bytes", "qr_allreduce_staged",
+           "qr_allreduce_staged_noalloc", "qr_host_workspace_bytes", "qr_allreduce_host")
+MAX_ELEMS = 1 << 36  # QR_MAX_ELEMS: the largest message (elements)
 DEFAULT_HOST_CHUNK = 1 << 22  # elements per rank per chunk of qr_allreduce_host (8 MiB of fp16)
 
 _lib = None
@@ -69,12 +70,12 @@ def lib():
                 L.qr_status_string.argtypes = [i]
                 L.qr_device_error.restype = i
                 L.qr_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i]
-                L.qr_direct_limit.restype = sz
-                L.qr_direct_limit.argtypes = []
-                L.qr_set_direct_limit.restype = None
-                L.qr_set_direct_limit.argtypes = [sz]
-                L.qr_selected_direct_limit.restype = sz
-                L.qr_selected_direct_limit.argtypes = [i, i, i, i]
+                L.qr_kernel_path.restype = i
+                L.qr_kernel_path.argtypes = [i, i, i, i, sz]
+                L.qr_set_kernel_path.restype = i
+                L.qr_set_kernel_path.argtypes = [i]
+                L.qr_forced_kernel_path.restype = i
+                L.qr_forced_kernel_path.argtypes = []
                 L.qr_stage1_bytes.restype = sz
                 L.qr_stage1_bytes.argtypes = [i, i, sz]
                 L.qr_allreduce_staged.restype = i
@@ -180,23 +181,40 @@ def qr_device_error(clear: bool = True) -> int:
     return int(flags.value)
 
 
-def qr_direct_limit() -> int:
-    """The process-wide direct-kernel limit override (elements per rank), or
-    DIRECT_LIMIT_TABLE when the measured per-shape table routes."""
-    return int(lib().qr_direct_limit())
+def qr_kernel_path(W: int, dtype, fmt: int, stages: int, n: int) -> int:
+    """The kernel a call of this shape and size runs now (PATH_DIRECT,
+    PATH_PIPELINE_NARROW or PATH_PIPELINE; stages 0: qr_quantize); -1 for a
+    shape no call can have."""
+    return int(lib().qr_kernel_path(W, _dtype_code(dtype), fmt, stages, n))
 
 
-def qr_set_direct_limit(n: int) -> None:
-    """Override the table for every call shape in the process (0: always the
-    pipeline; MAX_ELEMS: always the direct kernel); DIRECT_LIMIT_TABLE
-    restores the table.  Process-global: other threads are rerouted too."""
-    lib().qr_set_direct_limit(n)
+def qr_set_kernel_path(path: int) -> None:
+    """Force one kernel path for every call in the process (PATH_TABLE
+    restores the measured tables).  Process-global: other threads are
+    rerouted too."""
+    _check(lib().qr_set_kernel_path(path), "qr_set_kernel_path")
 
 
-def qr_selected_direct_limit(W: int, dtype, fmt: int, stages: int) -> int:
-    """The direct-kernel limit a call of this shape uses now (stages 0:
-    qr_quantize; 1, 2: the allreduce)."""
-    return int(lib().qr_selected_direct_limit(W, _dtype_code(dtype), fmt, stages))
+def qr_forced_kernel_path() -> int:
+    """The forced kernel path, or PATH_TABLE when the measured tables route."""
+    return int(lib().qr_forced_kernel_path())
+
+
+class forced_kernel_path:
+    """Context manager: force `path` for the calls inside, then restore the
+    previous setting (process-global, like qr_set_kernel_path)."""
+
+    def __init__(self, path: int):
+        self.path = path
+
+    def __enter__(self):
+        self.old = qr_forced_kernel_path()
+        qr_set_kernel_path(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        qr_set_kernel_path(self.old)
+        return False
 
 
 def qr_selftest_wait_timeout(limit_us: int, stream=None) -> None:

@@ -44,17 +44,22 @@ qr_status check_size(size_t n) {
 
 qr_status to_status(cudaError_t e) { return e == cudaSuccess ? QR_OK : QR_ERR_CUDA; }
 
-// Kernel-path selection: a process-wide override of the measured table
-// (QR_DIRECT_LIMIT_TABLE: none, the table routes).
-std::atomic<unsigned long long> g_direct_override{static_cast<unsigned long long>(QR_DIRECT_LIMIT_TABLE)};
+// Kernel-path selection: the measured tables, or a process-wide forced path
+// (QR_PATH_TABLE: none).
+std::atomic<int> g_forced_path{QR_PATH_TABLE};
 
 int world_index(int W) { return W == 1 ? 0 : W == 2 ? 1 : W == 4 ? 2 : 3; }
 
-// Messages of at most this many elements per rank take the direct kernel.
-unsigned long long direct_limit(int dt, int mode, int W, int fmt) {
-  const unsigned long long o = g_direct_override.load(std::memory_order_relaxed);
-  if (o != static_cast<unsigned long long>(QR_DIRECT_LIMIT_TABLE)) return o;
-  return kDirectLimitTable[dt][mode][world_index(W)][fmt];
+// The kernel a call of this shape and size runs: the direct kernel up to the
+// direct limit, the narrow-tile pipeline up to the narrow-tile limit, the
+// wide-tile pipeline beyond.
+int select_path(int dt, int mode, int W, int fmt, unsigned long long n) {
+  const int forced = g_forced_path.load(std::memory_order_relaxed);
+  if (forced != QR_PATH_TABLE) return forced;
+  const int w = world_index(W);
+  if (n <= kDirectLimitTable[dt][mode][w][fmt]) return QR_PATH_DIRECT;
+  if (n <= kNarrowTileLimitTable[dt][mode][w][fmt]) return QR_PATH_PIPELINE_NARROW;
+  return QR_PATH_PIPELINE;
 }
 
 cudaError_t dispatch_direct(int fmt, int dt, int mode, const PipeParams& p, cudaStream_t s) {
@@ -71,15 +76,17 @@ cudaError_t dispatch_direct(int fmt, int dt, int mode, const PipeParams& p, cuda
 }
 
 cudaError_t dispatch_pipeline(int fmt, int dt, int mode, const PipeParams& p, cudaStream_t s) {
-  if (p.n <= direct_limit(dt, mode, p.W, fmt)) return dispatch_direct(fmt, dt, mode, p, s);
+  const int path = select_path(dt, mode, p.W, fmt, p.n);
+  if (path == QR_PATH_DIRECT) return dispatch_direct(fmt, dt, mode, p, s);
+  const int cw = path == QR_PATH_PIPELINE_NARROW ? kNarrowTile : kWideTile;
   switch (fmt) {
-    case 0: return launch_pipeline_fmt_0(dt, mode, p, s);
-    case 1: return launch_pipeline_fmt_1(dt, mode, p, s);
-    case 2: return launch_pipeline_fmt_2(dt, mode, p, s);
-    case 3: return launch_pipeline_fmt_3(dt, mode, p, s);
-    case 4: return launch_pipeline_fmt_4(dt, mode, p, s);
-    case 5: return launch_pipeline_fmt_5(dt, mode, p, s);
-    case 6: return launch_pipeline_fmt_6(dt, mode, p, s);
+    case 0: return launch_pipeline_fmt_0(dt, mode, cw, p, s);
+    case 1: return launch_pipeline_fmt_1(dt, mode, cw, p, s);
+    case 2: return launch_pipeline_fmt_2(dt, mode, cw, p, s);
+    case 3: return launch_pipeline_fmt_3(dt, mode, cw, p, s);
+    case 4: return launch_pipeline_fmt_4(dt, mode, cw, p, s);
+    case 5: return launch_pipeline_fmt_5(dt, mode, cw, p, s);
+    case 6: return launch_pipeline_fmt_6(dt, mode, cw, p, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -295,6 +302,7 @@ const char* qr_status_string(qr_status st) {
     case QR_ERR_CUDA: return "CUDA runtime error";
     case QR_ERR_DEVICE: return "a kernel gave up waiting on its pipeline";
     case QR_ERR_SCRATCH: return "the message needs more stage-1 space than the built-in scratch array holds";
+    case QR_ERR_PATH: return "not a kernel path (QR_PATH_TABLE, QR_PATH_DIRECT, QR_PATH_PIPELINE_NARROW, QR_PATH_PIPELINE)";
     default: return "unknown status";
   }
 }
@@ -317,7 +325,6 @@ qr_status qr_quantize(qr_dtype dt, qr_format fmt, const void* in, size_t n, void
   p.W = 1;
   p.n = n;
   p.nb = (n + 31) / 32;
-  p.ntiles = (n + kTileElems - 1) / kTileElems;
   encoded_regions(f, n, enc, &p.codes, &p.scales, &p.zps, &p.fp_values);
   p.err = device_error_word();
   if (!p.err) return QR_ERR_CUDA;
@@ -381,7 +388,6 @@ qr_status qr_allreduce_emulated(int W, qr_dtype dt, qr_format fmt, int stages, c
   p.W = W;
   p.n = n;
   p.nb = (n + 31) / 32;
-  p.ntiles = (n + kTileElems - 1) / kTileElems;
   p.out = out;
   if (stages == 2) encoded_regions(f, n, wire, &p.codes, &p.scales, &p.zps, &p.fp_values);
   p.err = device_error_word();
@@ -494,7 +500,6 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages, const
     p.W = W;
     p.n = cn;
     p.nb = nbc;
-    p.ntiles = (cn + kTileElems - 1) / kTileElems;
     p.out = d_out;
     if (stages == 2 && host_wire) encoded_regions(f, cn, d_wire, &p.codes, &p.scales, &p.zps, &p.fp_values);
     p.err = err;
@@ -525,21 +530,26 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages, const
   return QR_OK;
 }
 
-size_t qr_direct_limit(void) { return static_cast<size_t>(g_direct_override.load()); }
-
-void qr_set_direct_limit(size_t n) { g_direct_override.store(static_cast<unsigned long long>(n)); }
-
-size_t qr_selected_direct_limit(int W, qr_dtype dt, qr_format fmt, int stages) {
+int qr_kernel_path(int W, qr_dtype dt, qr_format fmt, int stages, size_t n) {
   const int d = static_cast<int>(dt), f = static_cast<int>(fmt);
-  if (!valid_format(f) || stages < 0 || stages > 2) return 0;
+  if (!valid_format(f) || stages < 0 || stages > 2) return -1;
   if (stages == 0) {  // qr_quantize: one rank, fp16 or bf16
-    if (!valid_dtype(d)) return 0;
-    return static_cast<size_t>(direct_limit(d, MODE_ENCODE, 1, f));
+    if (!valid_dtype(d)) return -1;
+    return select_path(d, MODE_ENCODE, 1, f, n);
   }
-  if (!valid_dtype(d) && d != DT_BF16_AS_F16) return 0;
-  if (W != 1 && W != 2 && W != 4 && W != 8) return 0;
-  return static_cast<size_t>(direct_limit(d, stages == 1 ? MODE_AR1 : MODE_AR2, W, f));
+  if (!valid_dtype(d) && d != DT_BF16_AS_F16) return -1;
+  if (W != 1 && W != 2 && W != 4 && W != 8) return -1;
+  return select_path(d, stages == 1 ? MODE_AR1 : MODE_AR2, W, f, n);
 }
+
+qr_status qr_set_kernel_path(int path) {
+  if (path != QR_PATH_TABLE && path != QR_PATH_DIRECT && path != QR_PATH_PIPELINE_NARROW && path != QR_PATH_PIPELINE)
+    return QR_ERR_PATH;
+  g_forced_path.store(path);
+  return QR_OK;
+}
+
+int qr_forced_kernel_path(void) { return g_forced_path.load(); }
 
 qr_status qr_selftest_wait_timeout(unsigned int limit_us, void* stream) {
   if (limit_us == 0 || limit_us > 1000000u) return QR_ERR_SIZE;

@@ -63,7 +63,7 @@ cudaError_t resident_ctas(void (*kern)(Params), int threads, int smem, std::atom
   return cudaSuccess;
 }
 
-template <int F, int D, int M, int WS>
+template <int F, int D, int M, int WS, int CW>
 cudaError_t launch_pipe_w(const PipeParams& p, cudaStream_t s) {
   // Resident CTAs of this instantiation on each device, computed once per
   // device after its shared-memory limit is raised (resident_ctas' atomic
@@ -73,16 +73,18 @@ cudaError_t launch_pipe_w(const PipeParams& p, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  auto kern = qr_pipeline_kernel<F, D, M, WS>;
+  auto kern = qr_pipeline_kernel<F, D, M, WS, CW>;
+  constexpr int kSmem = kSmemBytesOf<M, CW>;
   if (cap[dev].load(std::memory_order_acquire) == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesOf<M>);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
   }
   unsigned long long max_grid = 0;
-  e = resident_ctas(kern, kThreads, kSmemBytesOf<M>, cap, &max_grid);
+  e = resident_ctas(kern, Tile<CW>::threads, kSmem, cap, &max_grid);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(p.ntiles < max_grid ? p.ntiles : max_grid);
-  return launch_overlapped(kern, grid, kThreads, kSmemBytesOf<M>, s, p);
+  const unsigned long long ntiles = (p.n + Tile<CW>::elems - 1) / Tile<CW>::elems;
+  const unsigned grid = static_cast<unsigned>(ntiles < max_grid ? ntiles : max_grid);
+  return launch_overlapped(kern, grid, Tile<CW>::threads, kSmem, s, p);
 }
 
 // The rank count is a compile-time constant in every instantiation (W is
@@ -94,19 +96,27 @@ cudaError_t launch_pipe_w(const PipeParams& p, cudaStream_t s) {
 template <int F, int D, int M>
 constexpr int kW8Of = M == MODE_AR2 ? 0 : 8;
 
-template <int F, int D, int M>
+// Narrow tiles (CW = 4) are built for W <= 4 only: at W = 8 they measured
+// slower from 16 MiB per rank up, and below that the direct kernel serves
+// W = 8; a W = 8 call asked for narrow tiles gets wide ones.
+template <int F, int D, int M, int CW>
 cudaError_t launch_pipe(const PipeParams& p, cudaStream_t s) {
   if constexpr (M == MODE_ENCODE) {
-    return launch_pipe_w<F, D, M, 1>(p, s);
+    return launch_pipe_w<F, D, M, 1, CW>(p, s);
   } else {
     switch (p.W) {
-      case 1: return launch_pipe_w<F, D, M, 1>(p, s);
-      case 2: return launch_pipe_w<F, D, M, 2>(p, s);
-      case 4: return launch_pipe_w<F, D, M, 4>(p, s);
-      case 8: return launch_pipe_w<F, D, M, kW8Of<F, D, M>>(p, s);
+      case 1: return launch_pipe_w<F, D, M, 1, CW>(p, s);
+      case 2: return launch_pipe_w<F, D, M, 2, CW>(p, s);
+      case 4: return launch_pipe_w<F, D, M, 4, CW>(p, s);
+      case 8: return launch_pipe_w<F, D, M, kW8Of<F, D, M>, kWideTile>(p, s);
       default: return cudaErrorInvalidValue;
     }
   }
+}
+
+template <int F, int D, int M>
+cudaError_t launch_pipe_cw(int cw, const PipeParams& p, cudaStream_t s) {
+  return cw == kNarrowTile ? launch_pipe<F, D, M, kNarrowTile>(p, s) : launch_pipe<F, D, M, kWideTile>(p, s);
 }
 
 // The direct kernel at W = 8 gets one CTA per 256 chunks, so each warp makes
@@ -190,21 +200,21 @@ cudaError_t QR_CAT(launch_staged_fmt_, QR_FMT)(int dt, const StagedParams& p, co
   return launch_stg<F, DT_BF16>(p, dp, s);
 }
 
-cudaError_t QR_CAT(launch_pipeline_fmt_, QR_FMT)(int dt, int mode, const PipeParams& p, cudaStream_t s) {
+cudaError_t QR_CAT(launch_pipeline_fmt_, QR_FMT)(int dt, int mode, int cw, const PipeParams& p, cudaStream_t s) {
   constexpr int F = QR_FMT;
   if (dt == DT_BF16_AS_F16) {  // allreduce modes only
-    if (mode == MODE_AR1) return launch_pipe<F, DT_BF16_AS_F16, MODE_AR1>(p, s);
-    if (mode == MODE_AR2) return launch_pipe<F, DT_BF16_AS_F16, MODE_AR2>(p, s);
+    if (mode == MODE_AR1) return launch_pipe_cw<F, DT_BF16_AS_F16, MODE_AR1>(cw, p, s);
+    if (mode == MODE_AR2) return launch_pipe_cw<F, DT_BF16_AS_F16, MODE_AR2>(cw, p, s);
     return cudaErrorInvalidValue;
   }
   if (dt == DT_F16) {
-    if (mode == MODE_ENCODE) return launch_pipe<F, DT_F16, MODE_ENCODE>(p, s);
-    if (mode == MODE_AR1) return launch_pipe<F, DT_F16, MODE_AR1>(p, s);
-    return launch_pipe<F, DT_F16, MODE_AR2>(p, s);
+    if (mode == MODE_ENCODE) return launch_pipe_cw<F, DT_F16, MODE_ENCODE>(cw, p, s);
+    if (mode == MODE_AR1) return launch_pipe_cw<F, DT_F16, MODE_AR1>(cw, p, s);
+    return launch_pipe_cw<F, DT_F16, MODE_AR2>(cw, p, s);
   }
-  if (mode == MODE_ENCODE) return launch_pipe<F, DT_BF16, MODE_ENCODE>(p, s);
-  if (mode == MODE_AR1) return launch_pipe<F, DT_BF16, MODE_AR1>(p, s);
-  return launch_pipe<F, DT_BF16, MODE_AR2>(p, s);
+  if (mode == MODE_ENCODE) return launch_pipe_cw<F, DT_BF16, MODE_ENCODE>(cw, p, s);
+  if (mode == MODE_AR1) return launch_pipe_cw<F, DT_BF16, MODE_AR1>(cw, p, s);
+  return launch_pipe_cw<F, DT_BF16, MODE_AR2>(cw, p, s);
 }
 
 cudaError_t QR_CAT(launch_direct_fmt_, QR_FMT)(int dt, int mode, const PipeParams& p, cudaStream_t s) {

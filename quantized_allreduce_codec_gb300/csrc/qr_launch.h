@@ -11,11 +11,12 @@
 
 namespace qr {
 
-// Launch the pipeline kernel or the direct (small-message) kernel (encode /
-// one-stage / two-stage) of format F for dtype dt, or the decode kernel;
-// grids sized for the current device.
-#define QR_DECLARE_FMT(N)                                                                   \
-  cudaError_t launch_pipeline_fmt_##N(int dt, int mode, const PipeParams& p, cudaStream_t s); \
+// Launch the pipeline kernel (cw consumer warps per CTA: kWideTile or
+// kNarrowTile) or the direct (small-message) kernel (encode / one-stage /
+// two-stage) of format F for dtype dt, or the decode kernel; grids sized for
+// the current device.
+#define QR_DECLARE_FMT(N)                                                                           \
+  cudaError_t launch_pipeline_fmt_##N(int dt, int mode, int cw, const PipeParams& p, cudaStream_t s); \
   cudaError_t launch_direct_fmt_##N(int dt, int mode, const PipeParams& p, cudaStream_t s);   \
   cudaError_t launch_decode_fmt_##N(int dt, const DecodeParams& p, cudaStream_t s);            \
   cudaError_t launch_staged_fmt_##N(int dt, const StagedParams& p, const DecodeParams& dp, cudaStream_t s);

@@ -1,21 +1,24 @@
 """Kernel-path selection table: from a measured sweep to csrc/qr_select_table.h.
 
-Every qr_quantize and qr_allreduce_emulated call is served by one of two
+Every qr_quantize and qr_allreduce_emulated call is served by one of three
 kernels that compute identical bits: the direct kernel (one memory round
-trip, lowest latency) and the persistent bulk-copy pipeline (highest
-bandwidth).  Which is faster at a given message size depends on the call's
-shape -- dtype, stage mode (encode-only, one-stage, two-stage), rank count W
-and format -- so the library routes by a per-shape size limit: messages of at
-most `limit` elements per rank take the direct kernel.  This is the GB300
+trip, lowest latency), the persistent bulk-copy pipeline with narrow (8 KiB)
+tiles and the same pipeline with wide (16 KiB) tiles (highest bandwidth).
+Which is fastest at a given message size depends on the call's shape --
+dtype, stage mode (encode-only, one-stage, two-stage), rank count W and
+format -- so the library routes by two per-shape size limits: messages of at
+most the direct limit (elements per rank) take the direct kernel, those of at
+most the narrow-tile limit the narrow-tile pipeline, longer ones the
+wide-tile pipeline.  This is the GB300
 counterpart of the per-(dtype, world size) size thresholds that the vLLM
 quick_all_reduce page keeps in _QR_MIN_SIZE, and of the size rule in vLLM PR
 #18473's description (custom allreduce for small messages, quick allreduce
 above), applied to the choice this one-GPU data path actually has.
 
-The sweep (``python bench.py --select-sweep OUT.json``) times both kernels at
-every size of a grid for every shape; this module picks, per shape, the limit
-that minimises the summed relative excess time over the grid, and writes the
-table as a C header that libqr.so compiles in.  Usage:
+The sweep (``python bench.py --select-sweep OUT.json``) times the kernels at
+every size of a grid for every shape; this module picks, per shape, the pair
+of limits that minimises the summed relative excess time over the grid, and
+writes the tables as a C header that libqr.so compiles in.  Usage:
 
     python -m quantized_allreduce_codec_gb300.select_table [SWEEP.json]
 
@@ -45,24 +48,40 @@ def valid_shape(dt: int, mode: int, W: int) -> bool:
     return True
 
 
-def choose_limit(points) -> int:
-    """points: [(n, t_direct, t_pipeline)] over a size grid.  The limit L (n <=
-    L: direct) among 0 and the grid sizes that minimises the sum over the grid
-    of t_routed / t_best - 1; ties go to the smaller limit.  A limit at the
-    largest size measured means the direct kernel won there too: it is
-    extended to every size."""
+def choose_limits(points) -> tuple:
+    """points: [(n, t_direct, t_narrow, t_wide)] over a size grid (t_narrow
+    None where the narrow-tile pipeline was not measured).  The limits
+    (L1, L2), L1 <= L2, among 0 and the grid sizes -- n <= L1: direct; n <= L2:
+    narrow tiles; else wide tiles -- that minimise the sum over the grid of
+    t_routed / t_best - 1; ties go to the smaller limits.  A limit at the
+    largest size measured means that path won there too: it is extended to
+    every size."""
     pts = sorted(points)
-    best_cost, best_L = None, 0
-    for L in [0] + [n for n, _, _ in pts]:
-        cost = 0.0
-        for n, td, tp in pts:
-            t = td if n <= L else tp
-            cost += t / min(td, tp) - 1.0
-        if best_cost is None or cost < best_cost - 1e-12:
-            best_cost, best_L = cost, L
-    if pts and best_L == pts[-1][0]:
-        best_L = MAX_ELEMS
-    return best_L
+    narrow = all(p[2] is not None for p in pts)
+    cands = [0] + [p[0] for p in pts]
+    best = None
+    for L1 in cands:
+        for L2 in (cands if narrow else [L1]):
+            if L2 < L1:
+                continue
+            cost = 0.0
+            for n, td, tn, tw in pts:
+                t = td if n <= L1 else tn if n <= L2 else tw
+                cost += t / min(x for x in (td, tn, tw) if x is not None) - 1.0
+            if best is None or cost < best[0] - 1e-12:
+                best = (cost, L1, L2)
+    _, L1, L2 = best if best else (0.0, 0, 0)
+    top = pts[-1][0] if pts else None
+    if L1 == top:
+        L1 = L2 = MAX_ELEMS
+    elif L2 == top:
+        L2 = MAX_ELEMS
+    return L1, L2
+
+
+def choose_limit(points) -> int:
+    """The direct limit alone, for points [(n, t_direct, t_pipeline)]."""
+    return choose_limits([(n, td, None, tp) for n, td, tp in points])[0]
 
 
 def records_of(data: dict) -> list:
@@ -73,17 +92,17 @@ def records_of(data: dict) -> list:
 
 
 def limits_from_sweep(records) -> dict:
-    """{(dt, mode, W, fmt): limit} from the sweep's records."""
+    """{(dt, mode, W, fmt): (direct limit, narrow-tile limit)} from the sweep's records."""
     by_shape = {}
     for r in records:
         key = (r["dt"], r["mode"], r["W"], r["fmt"])
-        by_shape.setdefault(key, []).append((r["n"], r["us_direct"], r["us_pipeline"]))
-    return {k: choose_limit(v) for k, v in by_shape.items()}
+        by_shape.setdefault(key, []).append((r["n"], r["us_direct"], r.get("us_narrow"), r["us_pipeline"]))
+    return {k: choose_limits(v) for k, v in by_shape.items()}
 
 
-def table(limits: dict) -> list:
-    """The 3 x 3 x 4 x 7 nested list compiled into the library (0 for shapes
-    no call can have)."""
+def table(limits: dict, which: int = 0) -> list:
+    """The 3 x 3 x 4 x 7 nested list of limit `which` (0: direct, 1: narrow
+    tiles) compiled into the library (0 for shapes no call can have)."""
     out = []
     for dt in DTYPES:
         a = []
@@ -95,49 +114,53 @@ def table(limits: dict) -> list:
                     if not valid_shape(dt, mode, W):
                         row.append(0)
                     else:
-                        row.append(int(limits.get((dt, mode, W, fmt), DEFAULT_LIMIT)))
+                        row.append(int(limits.get((dt, mode, W, fmt), (DEFAULT_LIMIT, DEFAULT_LIMIT))[which]))
                 b.append(row)
             a.append(b)
         out.append(a)
     return out
 
 
-def render(tab: list, source: str) -> str:
+def render(direct: list, narrow: list, source: str) -> str:
     lines = [
-        "// qr_select_table.h -- kernel-path selection table, GENERATED by",
+        "// qr_select_table.h -- kernel-path selection tables, GENERATED by",
         f"// quantized_allreduce_codec_gb300/select_table.py from {source}; do not edit.",
         "//",
-        "// kDirectLimitTable[dtype][mode][w][format]: messages of at most this many",
-        "// elements per rank take the direct kernel, longer ones the bulk-copy",
-        "// pipeline.  dtype: fp16, bf16, bf16 through fp16; mode: encode-only",
-        "// (qr_quantize), one-stage, two-stage; w: W = 1, 2, 4, 8; format: FP, Q8, Q6,",
-        "// Q4, FP8, Q8A, Q4A.  2^36 (the largest message) = always the direct kernel;",
-        "// 0 for shapes no call can have.  Chosen per shape from both kernels' times",
-        "// over a size grid on GB300 (the limit minimising the summed relative excess).",
+        "// [dtype][mode][w][format]: messages of at most kDirectLimitTable elements",
+        "// per rank take the direct kernel, those of at most kNarrowTileLimitTable",
+        "// the narrow-tile pipeline, longer ones the wide-tile pipeline.  dtype:",
+        "// fp16, bf16, bf16 through fp16; mode: encode-only (qr_quantize), one-stage,",
+        "// two-stage; w: W = 1, 2, 4, 8; format: FP, Q8, Q6, Q4, FP8, Q8A, Q4A.  2^36",
+        "// (the largest message) = every size; 0 for shapes no call can have.",
+        "// Chosen per shape from the kernels' times over a size grid on GB300 (the",
+        "// limits minimising the summed relative excess).",
         "#pragma once",
         "",
         "namespace qr {",
         "",
-        "static constexpr unsigned long long kDirectLimitTable[3][3][4][7] = {",
     ]
     dnames, mnames = ("fp16", "bf16", "bf16 through fp16"), ("encode", "one-stage", "two-stage")
-    for di, a in enumerate(tab):
-        lines.append(f"    {{  // {dnames[di]}")
-        for mi, b in enumerate(a):
-            lines.append(f"        {{  // {mnames[mi]}")
-            for wi, row in enumerate(b):
-                vals = ", ".join(f"{v}ull" for v in row)
-                lines.append(f"            {{{vals}}},  // W={WORLDS[wi]}")
-            lines.append("        },")
-        lines.append("    },")
-    lines += ["};", "", "}  // namespace qr", ""]
+    for name, tab in (("kDirectLimitTable", direct), ("kNarrowTileLimitTable", narrow)):
+        lines.append(f"static constexpr unsigned long long {name}[3][3][4][7] = {{")
+        for di, a in enumerate(tab):
+            lines.append(f"    {{  // {dnames[di]}")
+            for mi, b in enumerate(a):
+                lines.append(f"        {{  // {mnames[mi]}")
+                for wi, row in enumerate(b):
+                    vals = ", ".join(f"{v}ull" for v in row)
+                    lines.append(f"            {{{vals}}},  // W={WORLDS[wi]}")
+                lines.append("        },")
+            lines.append("    },")
+        lines += ["};", ""]
+    lines += ["}  // namespace qr", ""]
     return "\n".join(lines)
 
 
 def generate(sweep_path: str = SWEEP) -> str:
     with open(sweep_path) as f:
         data = json.load(f)
-    return render(table(limits_from_sweep(records_of(data))), os.path.basename(sweep_path))
+    lim = limits_from_sweep(records_of(data))
+    return render(table(lim, 0), table(lim, 1), os.path.basename(sweep_path))
 
 
 def main(argv=None):

@@ -77,47 +77,46 @@ def test_encoded_bytes_table():
     assert qr.qr_encoded_bytes(9, 1000) == 0
 
 
-def table_from_header():
-    """kDirectLimitTable[dt][mode][w][fmt] parsed from the generated header."""
-    text = open(os.path.join(ROOT, "quantized_allreduce_codec_gb300", "csrc", "qr_select_table.h")).read()
-    body = text[text.index("kDirectLimitTable"):]
-    vals = [int(v) for v in re.findall(r"(\d+)ull", body)]
-    assert len(vals) == 3 * 3 * 4 * 7
-    return [[[vals[((d * 3 + m) * 4 + w) * 7:((d * 3 + m) * 4 + w) * 7 + 7] for w in range(4)]
-             for m in range(3)] for d in range(3)]
-
-
-def test_selected_limit_follows_the_table(L):
-    tab = table_from_header()
-    assert qr.qr_direct_limit() == qr.DIRECT_LIMIT_TABLE  # the table routes by default
-    for fmt in range(7):
-        for dt in (0, 1):  # qr_quantize: one rank, W ignored
-            assert qr.qr_selected_direct_limit(2, dt, fmt, 0) == tab[dt][0][0][fmt]
-        for dt in (0, 1, 2):
-            for wi, W in enumerate((1, 2, 4, 8)):
-                for stages in (1, 2):
-                    assert qr.qr_selected_direct_limit(W, dt, fmt, stages) == tab[dt][stages][wi][fmt]
+def test_kernel_path_follows_the_tables(L):
+    from select_table_util import expected_path, limits, parse_tables
+    tabs = parse_tables()
+    assert qr.qr_forced_kernel_path() == qr.PATH_TABLE  # the tables route by default
+    shapes = [(1, dt, fmt, 0) for dt in (0, 1) for fmt in range(7)]
+    shapes += [(W, dt, fmt, st) for W in (1, 2, 4, 8) for dt in (0, 1, 2) for fmt in range(7) for st in (1, 2)]
+    for W, dt, fmt, st in shapes:
+        l1, l2 = limits(tabs, W, dt, fmt, st)
+        assert l1 <= l2
+        for n in {8, l1, l1 + 8, l2, l2 + 8, qr.MAX_ELEMS}:
+            n = max(8, min(n, qr.MAX_ELEMS))
+            assert qr.qr_kernel_path(W, dt, fmt, st, n) == expected_path(tabs, W, dt, fmt, st, n), (W, dt, fmt, st, n)
     # shapes no call can have
-    assert qr.qr_selected_direct_limit(2, 2, 1, 0) == 0   # the cast option has no encode-only call
-    assert qr.qr_selected_direct_limit(3, 0, 1, 2) == 0
-    assert qr.qr_selected_direct_limit(2, 0, 7, 2) == 0
-    assert qr.qr_selected_direct_limit(2, 0, 1, 3) == 0
-    assert qr.qr_selected_direct_limit(2, 5, 1, 2) == 0
+    assert qr.qr_kernel_path(2, 2, 1, 0, 64) == -1   # the cast option has no encode-only call
+    assert qr.qr_kernel_path(3, 0, 1, 2, 64) == -1
+    assert qr.qr_kernel_path(2, 0, 7, 2, 64) == -1
+    assert qr.qr_kernel_path(2, 0, 1, 3, 64) == -1
+    assert qr.qr_kernel_path(2, 5, 1, 2, 64) == -1
 
 
-def test_direct_limit_override_is_process_wide_and_reversible(L):
-    old = qr.qr_direct_limit()
+def test_forced_path_is_process_wide_and_reversible(L):
+    old = qr.qr_forced_kernel_path()
     try:
-        qr.qr_set_direct_limit(12345)
-        assert qr.qr_direct_limit() == 12345
-        for W, dt, fmt, st in ((2, 0, 1, 2), (8, 1, 6, 1), (1, 0, 3, 0)):
-            assert qr.qr_selected_direct_limit(W, dt, fmt, st) == 12345
-        qr.qr_set_direct_limit(qr.DIRECT_LIMIT_TABLE)
-        tab = table_from_header()
-        assert qr.qr_selected_direct_limit(8, 1, 6, 1) == tab[1][1][3][6]
+        for path in (qr.PATH_DIRECT, qr.PATH_PIPELINE_NARROW, qr.PATH_PIPELINE):
+            qr.qr_set_kernel_path(path)
+            assert qr.qr_forced_kernel_path() == path
+            for W, dt, fmt, st, n in ((2, 0, 1, 2, 64), (8, 1, 6, 1, 1 << 30), (1, 0, 3, 0, 4096)):
+                assert qr.qr_kernel_path(W, dt, fmt, st, n) == path
+        with pytest.raises(qr.QRError, match="QR_ERR_PATH"):
+            qr.qr_set_kernel_path(3)
+        assert qr.qr_forced_kernel_path() == qr.PATH_PIPELINE   # unchanged by the refused value
+        with qr.forced_kernel_path(qr.PATH_DIRECT):
+            assert qr.qr_forced_kernel_path() == qr.PATH_DIRECT
+        assert qr.qr_forced_kernel_path() == qr.PATH_PIPELINE
+        qr.qr_set_kernel_path(qr.PATH_TABLE)
+        from select_table_util import expected_path, parse_tables
+        assert qr.qr_kernel_path(8, 0, 3, 1, 8192 * 8192) == expected_path(parse_tables(), 8, 0, 3, 1, 8192 * 8192)
     finally:
-        qr.qr_set_direct_limit(old)
-    assert qr.qr_direct_limit() == old
+        qr.qr_set_kernel_path(old)
+    assert qr.qr_forced_kernel_path() == old
 
 
 def test_status_strings(L):

@@ -53,12 +53,8 @@ def test_two_stage_beyond_2_31_elements(oracle_mod, fmt):
     out = torch.empty(n, dtype=torch.int16, device="cuda")
     wbytes = qr.qr_encoded_bytes(fmt, n)
     wire = torch.empty(wbytes, dtype=torch.uint8, device="cuda")
-    limit = qr.qr_direct_limit()
-    try:
-        qr.qr_set_direct_limit(0)  # the pipeline kernel
+    with qr.forced_kernel_path(qr.PATH_PIPELINE):
         qr.qr_allreduce_emulated(W, F16, fmt, 2, ins, n, out, wire)
-    finally:
-        qr.qr_set_direct_limit(limit)
 
     blocks = boundary_blocks(n, 9200 + fmt)
     sub = [gather_blocks(x, blocks) for x in xs]
@@ -83,13 +79,9 @@ def test_two_stage_beyond_2_31_elements(oracle_mod, fmt):
     # the direct kernel on the same inputs: the same output and payload
     out2 = torch.empty_like(out)
     wire2 = torch.empty_like(wire)
-    limit = qr.qr_direct_limit()
-    try:
-        qr.qr_set_direct_limit(qr.MAX_ELEMS)
+    with qr.forced_kernel_path(qr.PATH_DIRECT):
         qr.qr_allreduce_emulated(W, F16, fmt, 2, ins, n, out2, wire2)
         torch.cuda.synchronize()
-    finally:
-        qr.qr_set_direct_limit(limit)
     assert torch.equal(out2, out), "direct and pipeline kernels disagree"
     assert torch.equal(wire2, wire), "direct and pipeline payloads disagree"
 
@@ -108,3 +100,9 @@ def test_quantize_beyond_2_31_elements(oracle_mod):
     o_codes, o_scales, _ = split_encoded(o, fmt, sub.size)
     assert np.array_equal(g_codes[blocks], o_codes)
     assert np.array_equal(g_scales[blocks], o_scales)
+    # the direct encoder on the same message: the whole encoding bit for bit
+    enc2 = torch.empty_like(enc)
+    with qr.forced_kernel_path(qr.PATH_DIRECT):
+        qr.qr_quantize(F16, fmt, xd, n, enc2)
+        torch.cuda.synchronize()
+    assert torch.equal(enc2, enc), "direct and pipeline encoders disagree"

@@ -34,14 +34,14 @@ def library():
     assert qr.qr_device_error(clear=True) == 0, "a kernel raised its wait-limit flag"
 
 
-@pytest.fixture(params=["direct", "pipeline"])
+@pytest.fixture(params=["direct", "pipeline", "pipeline_narrow"])
 def path(request):
     """Run the test once through each kernel: the direct (small-message)
-    kernel and the bulk-copy pipeline kernel."""
-    old = qr.qr_direct_limit()
-    qr.qr_set_direct_limit(qr.MAX_ELEMS if request.param == "direct" else 0)
-    yield request.param
-    qr.qr_set_direct_limit(old)
+    kernel and the bulk-copy pipeline with wide and with narrow tiles."""
+    forced = {"direct": qr.PATH_DIRECT, "pipeline": qr.PATH_PIPELINE,
+              "pipeline_narrow": qr.PATH_PIPELINE_NARROW}[request.param]
+    with qr.forced_kernel_path(forced):
+        yield request.param
 
 
 def spread_values(rng, n, dtype, zero_blocks=True):
@@ -316,25 +316,21 @@ def test_full_compare_64MiB(oracle_mod, fmt, stages):
             assert_encoded_equal(wire, o_wire, fmt, wl.n)
 
 
-def test_direct_limit_default_and_paths_agree(oracle_mod):
-    """By default the measured table routes every call shape; both kernels
-    give the same bits on a message just past the old fixed 4M-element
-    limit."""
-    assert qr.qr_direct_limit() == qr.DIRECT_LIMIT_TABLE
+def test_paths_agree_past_the_table_limits(oracle_mod):
+    """By default the measured tables route every call shape; the three
+    kernels give the same bits on a message just past a wide tile."""
+    assert qr.qr_forced_kernel_path() == qr.PATH_TABLE
     rng = np.random.default_rng(7000)
     n = 4 * 1024 * 1024 + 8
     xs = [to_bits(rng.standard_normal(n).astype(np.float32), F16) for _ in range(2)]
-    old = qr.qr_direct_limit()
-    try:
-        for fmt in (Q8, Q6, Q4A):
-            qr.qr_set_direct_limit(0)
-            a, wa = gpu_allreduce(F16, fmt, 2, xs)
-            qr.qr_set_direct_limit(qr.MAX_ELEMS)
-            b, wb = gpu_allreduce(F16, fmt, 2, xs)
-            assert_bits_equal(a, b, "paths")
-            assert np.array_equal(wa, wb)
-    finally:
-        qr.qr_set_direct_limit(old)
+    for fmt in (Q8, Q6, Q4A):
+        res = []
+        for path in (qr.PATH_PIPELINE, qr.PATH_DIRECT, qr.PATH_PIPELINE_NARROW):
+            with qr.forced_kernel_path(path):
+                res.append(gpu_allreduce(F16, fmt, 2, xs))
+        for a, wa in res[1:]:
+            assert_bits_equal(res[0][0], a, "paths")
+            assert np.array_equal(res[0][1], wa)
 
 
 @pytest.mark.parametrize("n", [40, 8200, 3 * 8192 + 40])

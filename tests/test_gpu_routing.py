@@ -1,9 +1,10 @@
-"""The kernel-path table decides which kernel serves a call: a message of
-exactly the selected limit runs the direct kernel and one 8-element step past
-it the pipeline kernel (seen as the kernel node of a captured CUDA graph), for
-shapes of every mode; the override reroutes every shape and restoring the
-table undoes it."""
-import numpy as np
+"""The kernel-path tables decide which kernel serves a call: a message of
+exactly the direct limit runs the direct kernel, one 8-element step past it
+the narrow-tile pipeline where the shape has a narrow-tile range, and one
+step past the narrow-tile limit the wide-tile pipeline (seen as the kernel
+node of a captured CUDA graph, the pipeline's tile width being its last
+template argument), for shapes of every mode; a forced path reroutes every
+shape and restoring the tables undoes it."""
 import pytest
 import torch
 
@@ -67,18 +68,27 @@ def kernels_launched(fn):
         _dot_print(g, path)
         text = open(path).read()
     del g
-    names = sorted(set(re.findall(r"qr_(?:direct|encode|pipeline|decode)_kernel", text)))
+    names = set()
+    # demangled "qr_pipeline_kernel<3, 0, 2, 2, 4>" or mangled "qr_pipeline_kernelILi3ELi0E...E"
+    for m in re.finditer(r"qr_(direct|encode|pipeline|decode)_kernel(<[^>]*>|I(?:Li-?\d+E)+E)?", text):
+        names.add((m.group(1), tuple(int(v) for v in re.findall(r"-?\d+", m.group(2) or ""))))
     assert names, "no qr kernel node in the captured graph"
-    return names
+    return sorted(names)
 
 
 def path_of(names):
-    """The path a call took: the direct kernel (qr_encode_kernel for
-    encode-only calls) or the pipeline kernel."""
-    direct = any("qr_direct_kernel" in nm or "qr_encode_kernel" in nm for nm in names)
-    pipe = any("qr_pipeline_kernel" in nm for nm in names)
-    assert direct != pipe, names
-    return "direct" if direct else "pipeline"
+    """The path a call took: PATH_DIRECT (qr_direct_kernel, or qr_encode_kernel
+    for encode-only calls), else the pipeline with narrow or wide tiles (the
+    pipeline kernel's fifth template argument: consumer warps per tile)."""
+    kinds = {k for k, _ in names}
+    assert len(kinds) == 1, names
+    kind = kinds.pop()
+    if kind in ("direct", "encode"):
+        return qr.PATH_DIRECT
+    assert kind == "pipeline", names
+    widths = {a[4] for _, a in names if len(a) == 5}
+    assert len(widths) == 1, names
+    return qr.PATH_PIPELINE_NARROW if widths.pop() == 4 else qr.PATH_PIPELINE
 
 
 def run(W, dtype, fmt, stages, n, bufs):
@@ -103,28 +113,27 @@ SHAPES = [(1, F16, Q4, 0), (1, BF16, Q8A, 0), (2, F16, Q8, 2), (2, F16, FP, 1), 
 
 
 @pytest.mark.parametrize("W,dtype,fmt,stages", SHAPES)
-def test_routing_follows_the_table(bufs, W, dtype, fmt, stages):
-    assert qr.qr_direct_limit() == qr.DIRECT_LIMIT_TABLE
-    limit = qr.qr_selected_direct_limit(W, dtype, fmt, stages)
-    probes = []
-    if limit > 0:
-        n = min(limit, MAX_TEST_N) // 8 * 8
-        probes.append((n, "direct"))
-    if limit < MAX_TEST_N:
-        probes.append((limit + 8 if limit else 8192, "pipeline"))
-    for n, want in probes:
-        assert path_of(kernels_launched(run(W, dtype, fmt, stages, n, bufs))) == want, (n, limit)
+def test_routing_follows_the_tables(bufs, W, dtype, fmt, stages):
+    from select_table_util import expected_path, limits, parse_tables
+    assert qr.qr_forced_kernel_path() == qr.PATH_TABLE
+    tabs = parse_tables()
+    l1, l2 = limits(tabs, W, dtype, fmt, stages)
+    probes = sorted({n for n in (8, l1, l1 + 8, l2, l2 + 8) if 8 <= n <= MAX_TEST_N})
+    for n in probes:
+        want = expected_path(tabs, W, dtype, fmt, stages, n)
+        assert qr.qr_kernel_path(W, dtype, fmt, stages, n) == want
+        if want == qr.PATH_PIPELINE_NARROW and W == 8:
+            want = qr.PATH_PIPELINE  # narrow tiles are built for W <= 4 only
+        assert path_of(kernels_launched(run(W, dtype, fmt, stages, n, bufs))) == want, (n, l1, l2)
 
 
-def test_override_reroutes_every_shape_and_the_table_comes_back(bufs):
+def test_forced_path_reroutes_every_shape_and_the_tables_come_back(bufs):
     W, dtype, fmt, stages = 2, F16, Q8, 2
-    limit = qr.qr_selected_direct_limit(W, dtype, fmt, stages)
-    try:
-        qr.qr_set_direct_limit(0)
-        assert path_of(kernels_launched(run(W, dtype, fmt, stages, 4096, bufs))) == "pipeline"
-        qr.qr_set_direct_limit(qr.MAX_ELEMS)
-        assert path_of(kernels_launched(run(W, dtype, fmt, stages, 1 << 22, bufs))) == "direct"
-    finally:
-        qr.qr_set_direct_limit(qr.DIRECT_LIMIT_TABLE)
-    assert qr.qr_selected_direct_limit(W, dtype, fmt, stages) == limit
-    np.testing.assert_equal(qr.qr_direct_limit(), qr.DIRECT_LIMIT_TABLE)
+    sizes = (4096, 1 << 22, 1 << 25)
+    before = [qr.qr_kernel_path(W, dtype, fmt, stages, n) for n in sizes]
+    for path, n in ((qr.PATH_PIPELINE, 4096), (qr.PATH_PIPELINE_NARROW, 4096), (qr.PATH_DIRECT, 1 << 22)):
+        with qr.forced_kernel_path(path):
+            assert qr.qr_kernel_path(W, dtype, fmt, stages, n) == path
+            assert path_of(kernels_launched(run(W, dtype, fmt, stages, n, bufs))) == path
+    assert qr.qr_forced_kernel_path() == qr.PATH_TABLE
+    assert [qr.qr_kernel_path(W, dtype, fmt, stages, n) for n in sizes] == before

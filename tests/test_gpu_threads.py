@@ -29,9 +29,12 @@ g = torch.Generator(device="cuda")
 g.manual_seed(3)
 
 def pipeline_size(W, dt, fmt, stages):
-    # just past the routed direct-kernel limit (the pipeline kernel), capped
-    lim = qr.qr_selected_direct_limit(W, dt, fmt, stages)
-    return min(lim + 8, 1 << 24) if lim < (1 << 24) else 1 << 24
+    # the smallest power of two (at most 2^24 elements) that the tables route
+    # to a pipeline kernel, so that its first-call set-up is raced on
+    for k in range(12, 25):
+        if qr.qr_kernel_path(W, dt, fmt, stages, 1 << k) != qr.PATH_DIRECT:
+            return 1 << k
+    return 1 << 24
 
 # (kind, W, dtype, fmt, stages, n): allreduce, quantize or staged
 shapes = [("ar", 2, F16, Q8, 2, 40000),
