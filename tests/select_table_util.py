@@ -17,7 +17,7 @@ def parse_tables():
     text = open(HEADER).read()
     out = {}
     for name in ("kDirectLimitTable", "kNarrowTileLimitTable"):
-        body = text[text.index(name):]
+        body = text[text.index(name + "[3][3][4][7] = {"):]  # the definition, not a mention in a comment
         body = body[:body.index("};")]
         vals = [int(v) for v in re.findall(r"(\d+)ull", body)]
         assert len(vals) == 3 * 3 * 4 * 7, name
