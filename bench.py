@@ -943,8 +943,9 @@ def run_profile_case(args):
       each launched twice (the first launch warms up).
     w4-bf16-2048x4096-q4a: the W=4 bf16 2048x4096 workload's Q4A two-stage
       call on its own inputs, launched three times.
-    codec-32M:FMT: qr_quantize then qr_dequantize of a 32M-element fp16
-      N(0,1) message in format FMT, three times each.
+    codec-32M:FMT[:PATH]: qr_quantize then qr_dequantize of a 32M-element
+      fp16 N(0,1) message in format FMT, three times each; the encoder the
+      library routes to, or the one PATH names (direct, narrow, wide).
     staged-w2-32M:FMT: qr_allreduce_staged, W=2 fp16 N(0,1), 32M elements
       per rank, format FMT, three times.
     tp2-64MiB:FMT:STAGES: the tp2 table's largest size (W=2 fp16 N(0,1), 64
@@ -993,11 +994,15 @@ def run_profile_case(args):
         enc = torch.empty(encoded_bytes(fmt, n), dtype=torch.uint8, device=dev)
         out = torch.empty(n, dtype=torch.int16, device=dev)
         if name == "codec-32M":
-            for _ in range(3):
-                qr.qr_quantize(F16, fmt, xs[0], n, enc)
-                qr.qr_dequantize(F16, fmt, enc, n, out)
+            paths = {"direct": qr.PATH_DIRECT, "narrow": qr.PATH_PIPELINE_NARROW, "wide": qr.PATH_PIPELINE}
+            path = paths[rest[1]] if len(rest) > 1 else qr.qr_kernel_path(1, F16, fmt, 0, n)
+            with qr.forced_kernel_path(path):
+                for _ in range(3):
+                    qr.qr_quantize(F16, fmt, xs[0], n, enc)
+                    qr.qr_dequantize(F16, fmt, enc, n, out)
+                kernel = served_by(qr, 1, F16, fmt, 0, n)
             done.append({"call": f"quantize, dequantize {FORMAT_NAMES[fmt]}",
-                         "kernel": served_by(qr, 1, F16, fmt, 0, n) + ", qr_decode_kernel"})
+                         "kernel": f"{kernel} ({qr.PATH_NAMES[path]}), qr_decode_kernel"})
         else:
             st1 = torch.empty(qr.qr_stage1_bytes(2, fmt, n), dtype=torch.uint8, device=dev)
             for _ in range(3):
