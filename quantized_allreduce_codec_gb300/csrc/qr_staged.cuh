@@ -93,23 +93,24 @@ __device__ __forceinline__ BlockScale f32_block_scale(const float (&x)[32], int 
 }
 
 // Encode the four chunks of a block and store codes / scale / zero-point into
-// an encoded region (codes at codes + blk*cb, scale at scales[blk]).  The
-// block's code bytes are assembled in registers and written with the widest
-// aligned stores (32 B: two 16-byte stores; 16 B: one; Q6's 24 B: three
-// 8-byte stores).
-template <int F>
-__device__ __forceinline__ void encode_store_block(const float (&x)[32], const BlockScale& b, float one, bool fast, int nvalid,
-                                                   uint8_t* codes, uint16_t* scales, uint16_t* zps,
+// an encoded region (codes at codes + blk*cb, scale at scales[blk]); chunk(k,
+// x) puts chunk k's eight binary32 values in x.  The block's code bytes are
+// assembled in registers and written with the widest aligned stores (32 B:
+// two 16-byte stores; 16 B: one; Q6's 24 B: three 8-byte stores).
+template <int F, typename ChunkFn>
+__device__ __forceinline__ void encode_store_block(ChunkFn&& chunk, const BlockScale& b, float one, bool fast,
+                                                   int nvalid, uint8_t* codes, uint16_t* scales, uint16_t* zps,
                                                    unsigned long long blk) {
   uint32_t pk[4][2];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    float dec[8];
+    float x[8], dec[8];
     pk[k][0] = pk[k][1] = 0u;
+    chunk(k, x);
     if (fast)
-      encode8<F, true>(&x[8 * k], b, one, dec, pk[k]);
+      encode8<F, true>(x, b, one, dec, pk[k]);
     else
-      encode8<F, false>(&x[8 * k], b, one, dec, pk[k]);
+      encode8<F, false>(x, b, one, dec, pk[k]);
     if (FmtInfo<F>::asym && k >= nvalid) pk[k][0] = pk[k][1] = 0u;  // pad codes are 0
   }
   uint8_t* cp = codes + blk * FmtInfo<F>::code_bytes;
@@ -131,18 +132,6 @@ __device__ __forceinline__ void encode_store_block(const float (&x)[32], const B
   if (FmtInfo<F>::asym) zps[blk] = b.z_bits;
 }
 
-// Calls f(r) for the ranks r = 0 .. W-1 in order: fully unrolled when the
-// rank count WS is a compile-time constant, a runtime loop when WS is 0.
-template <int WS, typename Fn>
-__device__ __forceinline__ void for_ranks(int W, Fn&& f) {
-  if constexpr (WS > 0) {
-#pragma unroll
-    for (int r = 0; r < WS; ++r) f(r);
-  } else {
-    for (int r = 0; r < W; ++r) f(r);
-  }
-}
-
 // Number of valid 8-element chunks of block blk: 4 unless the block is the
 // message's ragged last one.  FULL asserts that blk lies wholly inside.
 template <bool FULL>
@@ -152,64 +141,55 @@ __device__ __forceinline__ int valid_chunks(unsigned long long n, unsigned long 
   return rem >= 32 ? 4 : static_cast<int>(rem / 8);
 }
 
-// Kernel 1: one thread per block; for every rank, load its 64 bytes, encode
-// the block and write it into slot (owner, rank).  scatter_block is one
-// block's work; WS is the rank count when it is known at compile time (2)
-// or 0, and FULL (used only with a known WS) that the block is complete.
-template <int F, int D, int WS, bool FULL>
-__device__ __forceinline__ void scatter_block(const StagedParams& p, unsigned long long blk) {
-  const int W = WS ? WS : p.W;
-    const int nvalid = valid_chunks<FULL>(p.n, blk);
-    const unsigned long long j = owner_of(blk, p.chunk_nb, W);
-    const unsigned long long local = blk - j * p.chunk_nb;
-    uint4 next[4];  // the next rank's block, loaded one rank ahead
+// Kernel 1: one thread per (rank, block) -- rank blockIdx.y, block
+// blockIdx.x * kStagedThreads + threadIdx.x -- in one pass: load the block's
+// 64 bytes, encode it and write it into slot (owner, rank) at the owner's
+// local block index.  No loop over ranks: the W ranks' blocks are W times as
+// many independent threads, each holding one block's loads.
+template <int F, int D, bool FULL>
+__device__ __forceinline__ void scatter_block(const StagedParams& p, int r, unsigned long long blk) {
+  const int nvalid = valid_chunks<FULL>(p.n, blk);
+  const unsigned long long j = owner_of(blk, p.chunk_nb, p.W);
+  const unsigned long long local = blk - j * p.chunk_nb;
+  uint8_t* slot = p.stage1 + (j * p.W + r) * p.slot_bytes;
+  const uint4* src = reinterpret_cast<const uint4*>(p.in[r]) + blk * 4;
+  uint4 raw[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) raw[k] = (FULL || k < nvalid) ? __ldg(src + k) : make_uint4(0u, 0u, 0u, 0u);
+  if constexpr (!FmtInfo<F>::quant) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      next[k] = k < nvalid ? __ldg(reinterpret_cast<const uint4*>(p.in[0]) + blk * 4 + k) : make_uint4(0u, 0u, 0u, 0u);
-    for_ranks<WS>(W, [&](int r) {
-      uint8_t* slot = p.stage1 + (j * W + r) * p.slot_bytes;
-      uint4 raw[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) raw[k] = next[k];
-      if (r + 1 < W) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          next[k] = k < nvalid ? __ldg(reinterpret_cast<const uint4*>(p.in[r + 1]) + blk * 4 + k)
-                               : make_uint4(0u, 0u, 0u, 0u);
-      }
-      if constexpr (!FmtInfo<F>::quant) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (k < nvalid) reinterpret_cast<uint4*>(slot + local * 64)[k] = raw[k];
-      } else {
-        bool fast;
-        const BlockScale b = raw_block_scale<F, D>(raw, nvalid, fast);
-        float x[32];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) widen8<D>(raw[k], &x[8 * k]);
-        encode_store_block<F>(x, b, p.one, fast, nvalid, slot,
-                              reinterpret_cast<uint16_t*>(slot + slot_scales_off<F>(p.chunk_nb)),
-                              reinterpret_cast<uint16_t*>(slot + slot_zps_off<F>(p.chunk_nb)), local);
-      }
-    });
+      if (FULL || k < nvalid) reinterpret_cast<uint4*>(slot + local * 64)[k] = raw[k];
+  } else {
+    bool fast;
+    const BlockScale b = raw_block_scale<F, D>(raw, nvalid, fast);
+    encode_store_block<F>([&](int k, float* x) { widen8<D>(raw[k], x); }, b, p.one, fast, nvalid, slot,
+                          reinterpret_cast<uint16_t*>(slot + slot_scales_off<F>(p.chunk_nb)),
+                          reinterpret_cast<uint16_t*>(slot + slot_zps_off<F>(p.chunk_nb)), local);
+  }
 }
 
-template <int F, int D, int WS>
+template <int F, int D>
 __global__ void __launch_bounds__(kStagedThreads) qr_scatter_encode_kernel(const __grid_constant__ StagedParams p) {
   wait_prior_grid();
   allow_next_grid();
-  const unsigned long long stride = (unsigned long long)gridDim.x * kStagedThreads;
-  const unsigned long long nb_full = p.n / 32;  // blocks holding 32 elements
-  for (unsigned long long blk = (unsigned long long)blockIdx.x * kStagedThreads + threadIdx.x; blk < p.nb;
-       blk += stride) {
-    if constexpr (WS > 0) {
-      if (blk < nb_full)
-        scatter_block<F, D, WS, true>(p, blk);
-      else
-        scatter_block<F, D, WS, false>(p, blk);
-    } else {
-      scatter_block<F, D, 0, false>(p, blk);
-    }
+  const int r = static_cast<int>(blockIdx.y);
+  const unsigned long long blk = static_cast<unsigned long long>(blockIdx.x) * kStagedThreads + threadIdx.x;
+  if (blk < p.n / 32)
+    scatter_block<F, D, true>(p, r, blk);
+  else if (blk < p.nb)
+    scatter_block<F, D, false>(p, r, blk);
+}
+
+// Calls f(r) for the ranks r = 0 .. W-1 in order: fully unrolled when the
+// rank count WS is a compile-time constant, a runtime loop when WS is 0.
+template <int WS, typename Fn>
+__device__ __forceinline__ void for_ranks(int W, Fn&& f) {
+  if constexpr (WS > 0) {
+#pragma unroll
+    for (int r = 0; r < WS; ++r) f(r);
+  } else {
+    for (int r = 0; r < W; ++r) f(r);
   }
 }
 
@@ -252,8 +232,10 @@ __device__ __forceinline__ void load_slot_block(const uint8_t* slot, unsigned lo
 }
 
 // Kernel 2: one thread per block; the owner decodes the block from its W
-// source slots, sums them in rank order and requantizes into the payload
-// (reduce_block: one block; WS and FULL as for scatter_block).
+// source slots (each rank's loaded one rank ahead), sums them in rank order
+// and requantizes into the payload.  reduce_block is one block's work; WS is
+// the rank count when it is known at compile time (2, 4, 8) or 0, and FULL
+// (used only with a known WS) that the block is complete.
 template <int F, int D, int WS, bool FULL>
 __device__ __forceinline__ void reduce_block(const StagedParams& p, unsigned long long blk) {
   const int W = WS ? WS : p.W;
@@ -308,7 +290,12 @@ __device__ __forceinline__ void reduce_block(const StagedParams& p, unsigned lon
       }
       bool fast;
       const BlockScale b2 = f32_block_scale<F>(acc, nvalid, fast);
-      encode_store_block<F>(acc, b2, p.one, fast, nvalid, p.codes, p.scales, p.zps, blk);
+      encode_store_block<F>(
+          [&](int k, float* x) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = acc[8 * k + i];
+          },
+          b2, p.one, fast, nvalid, p.codes, p.scales, p.zps, blk);
     }
 }
 
