@@ -930,7 +930,8 @@ def run_select_sweep(args):
 # ----------------------------------------------------------------------------
 # small cases for a profiler (ncu): a few launches each, a few GB at most
 # ----------------------------------------------------------------------------
-PROFILE_CASES = ("step16M", "w4-bf16-2048x4096-q4a", "codec-32M:FMT", "staged-w2-32M:FMT", "tp2-64MiB:FMT:STAGES")
+PROFILE_CASES = ("step16M", "w4-bf16-2048x4096-q4a", "codec-32M:FMT", "staged-w2-32M:FMT", "staged-w8-16M:FMT",
+                 "tp2-64MiB:FMT:STAGES")
 
 
 def run_profile_case(args):
@@ -948,6 +949,8 @@ def run_profile_case(args):
       library routes to, or the one PATH names (direct, narrow, wide).
     staged-w2-32M:FMT: qr_allreduce_staged, W=2 fp16 N(0,1), 32M elements
       per rank, format FMT, three times.
+    staged-w8-16M:FMT: the same at W=8, 16M elements per rank (a quarter of
+      the W=8 8192x8192 workload).
     tp2-64MiB:FMT:STAGES: the tp2 table's largest size (W=2 fp16 N(0,1), 64
       MiB per rank, its seeded inputs), one call three times, routed by the
       library."""
@@ -986,11 +989,12 @@ def run_profile_case(args):
         for _ in range(3):
             qr.qr_allreduce_emulated(w.W, w.dtype, Q4A, 2, xs, w.n, out, wire)
         done.append({"call": "Q4A-2stage", "kernel": served_by(qr, w.W, w.dtype, Q4A, 2, w.n)})
-    elif name in ("codec-32M", "staged-w2-32M") and rest:
-        fmt, n = int(rest[0]), 32 << 20
+    elif name in ("codec-32M", "staged-w2-32M", "staged-w8-16M") and rest:
+        fmt = int(rest[0])
+        W, n = (8, 16 << 20) if name == "staged-w8-16M" else (2, 32 << 20)
         g = torch.Generator(device=dev)
         g.manual_seed(6)
-        xs = [torch.randn(n, device=dev, generator=g).half().view(torch.int16) for _ in range(2)]
+        xs = [torch.randn(n, device=dev, generator=g).half().view(torch.int16) for _ in range(W)]
         enc = torch.empty(encoded_bytes(fmt, n), dtype=torch.uint8, device=dev)
         out = torch.empty(n, dtype=torch.int16, device=dev)
         if name == "codec-32M":
@@ -1004,10 +1008,10 @@ def run_profile_case(args):
             done.append({"call": f"quantize, dequantize {FORMAT_NAMES[fmt]}",
                          "kernel": f"{kernel} ({qr.PATH_NAMES[path]}), qr_decode_kernel"})
         else:
-            st1 = torch.empty(qr.qr_stage1_bytes(2, fmt, n), dtype=torch.uint8, device=dev)
+            st1 = torch.empty(qr.qr_stage1_bytes(W, fmt, n), dtype=torch.uint8, device=dev)
             for _ in range(3):
-                qr.qr_allreduce_staged(2, F16, fmt, xs, n, out, enc, st1)
-            done.append({"call": f"staged {FORMAT_NAMES[fmt]}",
+                qr.qr_allreduce_staged(W, F16, fmt, xs, n, out, enc, st1)
+            done.append({"call": f"staged W={W} {FORMAT_NAMES[fmt]}",
                          "kernel": "qr_scatter_encode_kernel, qr_owner_reduce_kernel, qr_decode_kernel"})
     elif name == "tp2-64MiB" and len(rest) == 2:
         fmt, st = int(rest[0]), int(rest[1])
