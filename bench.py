@@ -359,9 +359,12 @@ class GpuTimer:
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e-3
 
-    def per_call_seconds(self, fn, reps):
-        """Device time of fn per call: [flush, fn] x reps minus [flush] x reps
-        (the median of three replays of each)."""
+    def per_call_seconds(self, fn, reps, pairs=7):
+        """Device time of fn per call: [flush, fn] x reps minus [flush] x reps.
+        The two graphs are replayed in turn `pairs` times and the median of
+        the paired differences is taken: the flush dominates every replay,
+        so a single difference carries the flush's run-to-run jitter (about
+        a tenth of a 10 us call)."""
         fn()  # eager first call: any one-time set-up happens outside capture
         self.torch.cuda.synchronize()
         g1 = self.capture(lambda: [(self.flush(), fn()) for _ in range(reps)])
@@ -370,10 +373,12 @@ class GpuTimer:
         g0 = self.flush_graphs[reps]
         for g in (g1, g0):
             g.replay()
-        t1 = statistics.median(self.replay_time(g1, 1) for _ in range(3))
-        t0 = statistics.median(self.replay_time(g0, 1) for _ in range(3))
+        diffs = []
+        for _ in range(pairs):
+            t1 = self.replay_time(g1, 1)
+            diffs.append(t1 - self.replay_time(g0, 1))
         del g1
-        return max((t1 - t0) / reps, 1e-9)
+        return max(statistics.median(diffs) / reps, 1e-9)
 
 
 def run_ours(args):
