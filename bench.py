@@ -256,22 +256,28 @@ def kernel_sources_sha256() -> str:
     """Hash of the kernel sources the committed ncu traffic was taken on."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("qr_device.cuh", "qr_kernels.cu", "qr_select_table.h"):
+    for f in ("qr_device.cuh", "qr_kernels.cu"):
         with open(os.path.join(ROOT, "quantized_allreduce_codec_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def recorded_traffic():
+def step_routes(qr, W: int, n: int) -> str:
+    """The kernel path of each call of the bench step, in step order."""
+    return ",".join(str(qr.qr_kernel_path(W, F16, fmt, st, n)) for fmt, st in STEP_CALLS)
+
+
+def recorded_traffic(routes: str):
     """DRAM bytes per launch per kernel from the committed ncu summary
     (lines key=value), if it was taken on the current kernel sources (matched
-    by hash); else None."""
+    by hash) with every call of the step on the kernel path it takes now;
+    else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             fields = dict(ln.strip().split("=", 1) for ln in f if "=" in ln and not ln.startswith("#"))
     except OSError:
         return None
-    if fields.get("sources_sha256") != kernel_sources_sha256():
+    if fields.get("sources_sha256") != kernel_sources_sha256() or fields.get("step_routes") != routes:
         return None
     return fields
 
@@ -522,7 +528,7 @@ def run_ours(args):
             got = out.cpu().numpy().view(np.uint16)[idx]
             errors[step_name(fmt, st)] = error_vs_exact(sub, got, wl.dtype, fmt, st)
         errors["sample"] = f"{idx.size // 32} random blocks ({idx.size} elements) of the message"
-    traffic = recorded_traffic()
+    traffic = recorded_traffic(step_routes(qr, W, n))
     t_key = f"{dominant}.bytes_per_launch"
     roofline = {"kernel": f"{dominant} (W={W}, fp16, 128 MiB per rank; {dk['launches']} of the step's "
                           f"{len(STEP_CALLS)} launches, routed to it by the measured kernel-path table: "
