@@ -228,9 +228,7 @@ size_t qr_host_workspace_bytes(int W, qr_format fmt, size_t chunk_elems);
  * The message is processed in chunks of chunk_elems elements (a multiple of
  * 32; the last chunk may be shorter), double-buffered in `workspace`: the
  * copy-in of chunk i+1, the kernel on chunk i and the copy-out of chunk i-1
- * run at the same time on the two copy directions and the SMs.  A chunk's W
- * rank copies are spread over up to four internal copy streams, so several
- * copy engines move them at once.
+ * run at the same time on the two copy directions and the SMs.
  *   host_inputs  host array of W host pointers, n values of dtype dt each,
  *                read only; any alignment
  *   host_out     host, n values of dtype dt, written

@@ -158,44 +158,35 @@ __global__ void qr_selftest_wait_kernel(unsigned* err, unsigned long long limit_
 }
 
 // ---- qr_allreduce_host: per-device copy streams and reusable events ----
-// Chunk i uses buffer i & 1.  Its W rank copies go round-robin over
-// kCopyInStreams streams, so several copy engines move them at once;
-// in_done[b][c]: stream c's copies of it finished; k_done[b]: its kernel
-// finished (the inputs may be overwritten); out_done[b]: its copy-out
-// finished (the output may be overwritten).
-constexpr int kCopyInStreams = 4;
+// Chunk i uses buffer i & 1.  in_done[b]: its copy-in finished; k_done[b]:
+// its kernel finished (the inputs may be overwritten); out_done[b]: its
+// copy-out finished (the output may be overwritten).
 struct HostPipe {
   bool ready = false;
-  cudaStream_t s_in[kCopyInStreams] = {}, s_out = nullptr;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
   cudaEvent_t start = nullptr;
-  cudaEvent_t in_done[2][kCopyInStreams] = {}, k_done[2] = {nullptr, nullptr}, out_done[2] = {nullptr, nullptr};
+  cudaEvent_t in_done[2] = {nullptr, nullptr}, k_done[2] = {nullptr, nullptr}, out_done[2] = {nullptr, nullptr};
 };
 HostPipe g_host_pipe[kMaxDevices];
 std::mutex g_host_mutex[kMaxDevices];
 
 cudaError_t host_pipe_ready(HostPipe& h) {
   if (h.ready) return cudaSuccess;
-  cudaError_t e = cudaSuccess;
-  for (int c = 0; c < kCopyInStreams && e == cudaSuccess; ++c)
-    e = cudaStreamCreateWithFlags(&h.s_in[c], cudaStreamNonBlocking);
+  cudaError_t e = cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
   for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
-    for (int c = 0; c < kCopyInStreams && e == cudaSuccess; ++c)
-      e = cudaEventCreateWithFlags(&h.in_done[b][c], cudaEventDisableTiming);
+    e = cudaEventCreateWithFlags(&h.in_done[b], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.k_done[b], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.out_done[b], cudaEventDisableTiming);
   }
   if (e != cudaSuccess) {  // release what was made; the next call tries again
-    for (cudaStream_t st : h.s_in)
-      if (st) cudaStreamDestroy(st);
+    if (h.s_in) cudaStreamDestroy(h.s_in);
     if (h.s_out) cudaStreamDestroy(h.s_out);
-    cudaEvent_t* evs[] = {&h.start, &h.k_done[0], &h.k_done[1], &h.out_done[0], &h.out_done[1]};
+    cudaEvent_t* evs[] = {&h.start, &h.in_done[0], &h.in_done[1], &h.k_done[0], &h.k_done[1], &h.out_done[0],
+                          &h.out_done[1]};
     for (cudaEvent_t* ev : evs)
       if (*ev) cudaEventDestroy(*ev);
-    for (auto& row : h.in_done)
-      for (cudaEvent_t ev : row)
-        if (ev) cudaEventDestroy(ev);
     h = HostPipe();
     return e;
   }
@@ -478,10 +469,9 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages, const
   do {                                             \
     if ((call) != cudaSuccess) return QR_ERR_CUDA; \
   } while (0)
-  // the copy streams start after the work already on `stream`
-  const int ncopy = W < kCopyInStreams ? W : kCopyInStreams;  // copy-in streams this call uses
+  // both copy streams start after the work already on `stream`
   QR_TRY(cudaEventRecord(h.start, s));
-  for (int c = 0; c < ncopy; ++c) QR_TRY(cudaStreamWaitEvent(h.s_in[c], h.start, 0));
+  QR_TRY(cudaStreamWaitEvent(h.s_in, h.start, 0));
   QR_TRY(cudaStreamWaitEvent(h.s_out, h.start, 0));
   for (size_t i = 0; i < nchunks; ++i) {
     const int b = static_cast<int>(i & 1);
@@ -492,18 +482,16 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages, const
     const size_t cn = (n - c0) < chunk_elems ? (n - c0) : chunk_elems;
     const size_t blk0 = c0 / 32, nbc = (cn + 31) / 32;
 
-    // copy-in: buffer b is free once chunk i-2's kernel has read it; rank r
-    // goes on copy stream r mod ncopy
-    for (int c = 0; c < ncopy; ++c)
-      if (i >= 2) QR_TRY(cudaStreamWaitEvent(h.s_in[c], h.k_done[b], 0));
+    // copy-in: buffer b is free once chunk i-2's kernel has read it
+    if (i >= 2) QR_TRY(cudaStreamWaitEvent(h.s_in, h.k_done[b], 0));
     for (int r = 0; r < W; ++r)
       QR_TRY(cudaMemcpyAsync(base + r * pad256(chunk_elems * 2), static_cast<const uint8_t*>(host_inputs[r]) + c0 * 2,
-                             cn * 2, cudaMemcpyHostToDevice, h.s_in[r % ncopy]));
-    for (int c = 0; c < ncopy; ++c) QR_TRY(cudaEventRecord(h.in_done[b][c], h.s_in[c]));
+                             cn * 2, cudaMemcpyHostToDevice, h.s_in));
+    QR_TRY(cudaEventRecord(h.in_done[b], h.s_in));
 
     // kernel on the caller's stream: after the copy-in, and after chunk i-2's
     // copy-out has read this buffer's output and payload
-    for (int c = 0; c < ncopy; ++c) QR_TRY(cudaStreamWaitEvent(s, h.in_done[b][c], 0));
+    QR_TRY(cudaStreamWaitEvent(s, h.in_done[b], 0));
     if (i >= 2) QR_TRY(cudaStreamWaitEvent(s, h.out_done[b], 0));
     PipeParams p;
     std::memset(&p, 0, sizeof p);
