@@ -308,6 +308,17 @@ const char *qr_status_string(qr_status st);
  * qr_device_error().  Nothing faults and nothing hangs. */
 qr_status qr_selftest_wait_timeout(unsigned int limit_us, void *stream);
 
+/* Self-test of the block-scale reciprocal the direct kernel uses (two
+ * Newton-Raphson steps on the hardware approximation instead of the
+ * correctly rounded library reciprocal): writes, for every positive finite
+ * fp16 value s (bit patterns 1 .. 0x7BFF in order), the binary32 reciprocal
+ * the kernels would use for a block scale s, so that a test can compare all
+ * of them with the IEEE quotient 1/s that the method defines.
+ *   out     device, QR_SELFTEST_RECIPROCALS floats, 16-byte aligned, written
+ * QR_ERR_NULL / QR_ERR_ALIGN for a bad buffer; asynchronous on `stream`. */
+#define QR_SELFTEST_RECIPROCALS 0x7BFF
+qr_status qr_selftest_reciprocal(float *out, void *stream);
+
 /* Kernels never wait forever: a pipeline wait that exceeds its time limit
  * sets a flag in device memory and the kernel returns early.  This call
  * synchronises the current device, copies the flags to *flags (0 = none

@@ -29,7 +29,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqr.so")
 EXPORTS = ("qr_encoded_bytes", "qr_quantize", "qr_dequantize", "qr_allreduce_emulated",
            "qr_status_string", "qr_device_error", "qr_kernel_path", "qr_set_kernel_path",
-           "qr_forced_kernel_path", "qr_selftest_wait_timeout", "qr_stage1_bytes", "qr_allreduce_staged",
+           "qr_forced_kernel_path", "qr_selftest_wait_timeout", "qr_selftest_reciprocal", "qr_stage1_bytes", "qr_allreduce_staged",
            "qr_allreduce_staged_noalloc", "qr_host_workspace_bytes", "qr_allreduce_host")
 MAX_ELEMS = 1 << 36  # QR_MAX_ELEMS: the largest message (elements)
 DEFAULT_HOST_CHUNK = 1 << 22  # elements per rank per chunk of qr_allreduce_host (8 MiB of fp16)
@@ -88,6 +88,8 @@ def lib():
                 L.qr_allreduce_host.argtypes = [i, i, i, i, vp, sz, vp, vp, vp, sz, sz, vp]
                 L.qr_selftest_wait_timeout.restype = i
                 L.qr_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+                L.qr_selftest_reciprocal.restype = i
+                L.qr_selftest_reciprocal.argtypes = [vp, vp]
                 _lib = L
     return _lib
 
@@ -221,6 +223,17 @@ def qr_selftest_wait_timeout(limit_us: int, stream=None) -> None:
     """Launch the bounded-wait self-test (raises device flag 8 after limit_us)."""
     _check(lib().qr_selftest_wait_timeout(limit_us, _stream(stream)), "qr_selftest_wait_timeout")
 
+
+SELFTEST_RECIPROCALS = 0x7BFF
+
+
+def qr_selftest_reciprocal(out, stream=None) -> None:
+    """The direct kernel's block-scale reciprocal of every positive finite
+    fp16 value (bit patterns 1 .. 0x7BFF) into the float32 device tensor out
+    (at least SELFTEST_RECIPROCALS elements)."""
+    if out.numel() * out.element_size() < 4 * SELFTEST_RECIPROCALS:
+        raise ValueError("out holds fewer than SELFTEST_RECIPROCALS floats")
+    _check(lib().qr_selftest_reciprocal(_addr(out), _stream(stream)), "qr_selftest_reciprocal")
 
 def qr_stage1_bytes(W: int, fmt: int, n: int) -> int:
     """Bytes of the stage-1 exchange buffer of qr_allreduce_staged."""

@@ -157,6 +157,14 @@ __global__ void qr_selftest_wait_kernel(unsigned* err, unsigned long long limit_
   if (!__all_sync(0xffffffffu, completed) && threadIdx.x == 0) atomicOr(err, kErrSelfTest);
 }
 
+// The block-scale reciprocal of every positive finite fp16 value (bit
+// patterns 1 .. 0x7BFF, in order) into out.
+__global__ void qr_selftest_reciprocal_kernel(float* out) {
+  const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < QR_SELFTEST_RECIPROCALS)
+    out[i] = recip_of_half(__half2float(__ushort_as_half(static_cast<unsigned short>(i + 1))));
+}
+
 // ---- qr_allreduce_host: per-device copy streams and reusable events ----
 // Chunk i uses buffer i & 1.  in_done[b]: its copy-in finished; k_done[b]:
 // its kernel finished (the inputs may be overwritten); out_done[b]: its
@@ -557,6 +565,13 @@ qr_status qr_selftest_wait_timeout(unsigned int limit_us, void* stream) {
   if (!err) return QR_ERR_CUDA;
   qr_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       err, static_cast<unsigned long long>(limit_us) * 1000ull);
+  return to_status(cudaGetLastError());
+}
+
+qr_status qr_selftest_reciprocal(float* out, void* stream) {
+  if (!out) return QR_ERR_NULL;
+  if (!aligned16(out)) return QR_ERR_ALIGN;
+  qr_selftest_reciprocal_kernel<<<(QR_SELFTEST_RECIPROCALS + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(out);
   return to_status(cudaGetLastError());
 }
 

@@ -172,6 +172,8 @@ def test_codec_argument_errors(L):
     assert d(2, 1, A, 64, B, None) == 2
     assert qr.lib().qr_selftest_wait_timeout(0, None) == 6           # limit out of range
     assert qr.lib().qr_selftest_wait_timeout(1000001, None) == 6
+    assert qr.lib().qr_selftest_reciprocal(None, None) == 1         # no buffer
+    assert qr.lib().qr_selftest_reciprocal(A + 4, None) == 7         # misaligned
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
