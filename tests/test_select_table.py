@@ -36,6 +36,38 @@ def test_ties_go_to_the_smaller_limit():
     assert st.choose_limit([(1024, 1.0, 1.0), (2048, 1.0, 1.0)]) == 0
 
 
+def test_three_way_limits_are_the_two_crossovers_of_a_clean_sweep():
+    # direct fastest up to 1M elements, narrow tiles up to 16M, wide tiles beyond
+    def t(n):
+        return (1.0 if n <= 1 << 20 else 3.0, 2.0 if n <= 1 << 24 else 4.0, 2.5 if n <= 1 << 24 else 1.0)
+    pts = [(n, *t(n)) for n in (1 << k for k in range(10, 27))]
+    assert st.choose_limits(pts) == (1 << 20, 1 << 24)
+
+
+def test_narrow_tiles_that_never_win_get_an_empty_range():
+    pts = [(n, 1.0 if n <= 1 << 20 else 3.0, 2.5, 2.0) for n in (1 << k for k in range(10, 26))]
+    l1, l2 = st.choose_limits(pts)
+    assert l1 == 1 << 20 and l2 == l1
+
+
+def test_narrow_tiles_winning_at_the_largest_size_extend_to_every_size():
+    pts = [(n, 1.0 if n <= 1 << 20 else 3.0, 2.0, 2.5) for n in (1 << k for k in range(10, 26))]
+    assert st.choose_limits(pts) == (1 << 20, st.MAX_ELEMS)
+
+
+def test_without_narrow_timings_the_limits_coincide():
+    pts = [(n, 1.0 if n <= 1 << 18 else 2.0, None, 1.5) for n in (1 << k for k in range(10, 26))]
+    assert st.choose_limits(pts) == (1 << 18, 1 << 18)
+
+
+def test_tables_carry_both_limits():
+    lim = {(0, 2, 2, 3): (1 << 20, 1 << 24)}
+    assert st.table(lim, 0)[0][2][1][3] == 1 << 20
+    assert st.table(lim, 1)[0][2][1][3] == 1 << 24
+    text = st.render(st.table(lim, 0), st.table(lim, 1), "x.json")
+    assert "kDirectLimitTable[3][3][4][7]" in text and "kNarrowTileLimitTable[3][3][4][7]" in text
+
+
 def test_table_shape_and_impossible_shapes():
     tab = st.table({})
     assert len(tab) == 3 and all(len(a) == 3 for a in tab)
