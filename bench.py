@@ -287,7 +287,9 @@ def served_by(qr, W: int, dtype: int, fmt: int, stages: int, n: int) -> str:
     stages 0 = qr_quantize)."""
     path = qr.qr_kernel_path(W, dtype, fmt, stages, n)
     if path == qr.PATH_DIRECT:
-        return "qr_encode_kernel" if stages == 0 else "qr_direct_kernel"
+        if stages == 0:
+            return "qr_encode_kernel"
+        return "qr_block_kernel" if W == 2 and stages == 2 and fmt not in (FP, FP8) else "qr_direct_kernel"
     return "qr_pipeline_kernel"
 
 

@@ -124,18 +124,29 @@ cudaError_t launch_pipe_cw(int cw, const PipeParams& p, cudaStream_t s) {
 // earlier ones retire: on GB300 3-5 % faster from 4 MiB per rank up than a
 // grid of resident CTAs looping over the message.  At W = 2 and 4 the
 // resident grid measured as fast or faster (up to 5 % at 128 MiB) and stays.
+// The direct path's kernel: the block kernel (one thread per block) for the
+// W = 2 two-stage calls of the integer formats, else the four-lanes-per-block
+// direct kernel.
+template <int F, int M, int WS>
+constexpr bool kBlockKernelOf = WS == 2 && M == MODE_AR2 && FmtInfo<F>::quant && !FmtInfo<F>::fp8;
+
 template <int F, int D, int M, int WS>
 cudaError_t launch_dir_w(const PipeParams& p, cudaStream_t s) {
-  const unsigned long long want = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;  // at most 2^25
-  if constexpr (WS == 8) {
-    return launch_overlapped(qr_direct_kernel<F, D, M, WS>, static_cast<unsigned>(want), kDirectThreads, 0, s, p);
+  if constexpr (kBlockKernelOf<F, M, WS>) {  // one CTA per kBlockThreads blocks, one pass
+    const unsigned long long g = (p.nb + kBlockThreads - 1) / kBlockThreads;  // at most 2^24
+    return launch_overlapped(qr_block_kernel<F, D, M, WS>, static_cast<unsigned>(g), kBlockThreads, 0, s, p);
   } else {
-    static std::atomic<unsigned long long> cap[kMaxDevices];
-    unsigned long long max_grid = 0;
-    cudaError_t e = resident_ctas(qr_direct_kernel<F, D, M, WS>, kDirectThreads, 0, cap, &max_grid);
-    if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(want < max_grid ? want : max_grid);
-    return launch_overlapped(qr_direct_kernel<F, D, M, WS>, grid, kDirectThreads, 0, s, p);
+    const unsigned long long want = (p.nb * 4 + kDirectThreads - 1) / kDirectThreads;  // at most 2^25
+    if constexpr (WS == 8) {
+      return launch_overlapped(qr_direct_kernel<F, D, M, WS>, static_cast<unsigned>(want), kDirectThreads, 0, s, p);
+    } else {
+      static std::atomic<unsigned long long> cap[kMaxDevices];
+      unsigned long long max_grid = 0;
+      cudaError_t e = resident_ctas(qr_direct_kernel<F, D, M, WS>, kDirectThreads, 0, cap, &max_grid);
+      if (e != cudaSuccess) return e;
+      const unsigned grid = static_cast<unsigned>(want < max_grid ? want : max_grid);
+      return launch_overlapped(qr_direct_kernel<F, D, M, WS>, grid, kDirectThreads, 0, s, p);
+    }
   }
 }
 

@@ -70,20 +70,21 @@ def kernels_launched(fn):
     del g
     names = set()
     # demangled "qr_pipeline_kernel<3, 0, 2, 2, 4>" or mangled "qr_pipeline_kernelILi3ELi0E...E"
-    for m in re.finditer(r"qr_(direct|encode|pipeline|decode)_kernel(<[^>]*>|I(?:Li-?\d+E)+E)?", text):
+    for m in re.finditer(r"qr_(direct|block|encode|pipeline|decode)_kernel(<[^>]*>|I(?:Li-?\d+E)+E)?", text):
         names.add((m.group(1), tuple(int(v) for v in re.findall(r"-?\d+", m.group(2) or ""))))
     assert names, "no qr kernel node in the captured graph"
     return sorted(names)
 
 
 def path_of(names):
-    """The path a call took: PATH_DIRECT (qr_direct_kernel, or qr_encode_kernel
-    for encode-only calls), else the pipeline with narrow or wide tiles (the
+    """The path a call took: PATH_DIRECT (qr_direct_kernel; qr_block_kernel for
+    the W=2 two-stage calls of the integer formats; qr_encode_kernel for
+    encode-only calls), else the pipeline with narrow or wide tiles (the
     pipeline kernel's fifth template argument: consumer warps per tile)."""
     kinds = {k for k, _ in names}
     assert len(kinds) == 1, names
     kind = kinds.pop()
-    if kind in ("direct", "encode"):
+    if kind in ("direct", "block", "encode"):
         return qr.PATH_DIRECT
     assert kind == "pipeline", names
     widths = {a[4] for _, a in names if len(a) == 5}
