@@ -944,7 +944,7 @@ def run_select_sweep(args):
 # small cases for a profiler (ncu): a few launches each, a few GB at most
 # ----------------------------------------------------------------------------
 PROFILE_CASES = ("step16M", "w4-bf16-2048x4096-q4a", "codec-32M:FMT", "staged-w2-32M:FMT", "staged-w8-16M:FMT",
-                 "tp2-64MiB:FMT:STAGES")
+                 "tp2-<16|64>MiB:FMT:STAGES")
 
 
 def run_profile_case(args):
@@ -964,9 +964,9 @@ def run_profile_case(args):
       per rank, format FMT, three times.
     staged-w8-16M:FMT: the same at W=8, 16M elements per rank (a quarter of
       the W=8 8192x8192 workload).
-    tp2-64MiB:FMT:STAGES: the tp2 table's largest size (W=2 fp16 N(0,1), 64
-      MiB per rank, its seeded inputs), one call three times, routed by the
-      library."""
+    tp2-<16|64>MiB:FMT:STAGES: a size of the tp2 table (W=2 fp16 N(0,1), 16
+      or 64 MiB per rank, its seeded inputs), one call three times, routed
+      by the library."""
     import torch
 
     import quantized_allreduce_codec_gb300 as qr
@@ -1026,9 +1026,9 @@ def run_profile_case(args):
                 qr.qr_allreduce_staged(W, F16, fmt, xs, n, out, enc, st1)
             done.append({"call": f"staged W={W} {FORMAT_NAMES[fmt]}",
                          "kernel": "qr_scatter_encode_kernel, qr_owner_reduce_kernel, qr_decode_kernel"})
-    elif name == "tp2-64MiB" and len(rest) == 2:
+    elif name in ("tp2-16MiB", "tp2-64MiB") and len(rest) == 2:
         fmt, st = int(rest[0]), int(rest[1])
-        w = sweep_workload(TP2_BYTES)
+        w = sweep_workload((16 << 20) if name == "tp2-16MiB" else TP2_BYTES)
         xs = [torch.from_numpy(x.view(np.int16)).to(dev) for x in workload_inputs(w)]
         out = torch.empty(w.n, dtype=torch.int16, device=dev)
         wire = torch.empty(encoded_bytes(fmt, w.n), dtype=torch.uint8, device=dev)
