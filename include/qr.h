@@ -258,9 +258,11 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages,
                             void *stream);
 
 /* Kernel-path selection.  Every qr_quantize and qr_allreduce_emulated call is
- * served by one of three kernels that compute identical bits:
- *   QR_PATH_DIRECT           a single-pass kernel with one memory round trip
- *                            (lowest latency);
+ * served by one of three kernel paths that compute identical bits:
+ *   QR_PATH_DIRECT           single-pass kernels with one memory round trip
+ *                            (lowest latency): four lanes per block, or one
+ *                            thread per block for qr_quantize and for the W=2
+ *                            two-stage calls of the integer formats;
  *   QR_PATH_PIPELINE_NARROW  the persistent bulk-copy pipeline with 8 KiB tiles
  *                            (mid-size messages: a shorter first fill and
  *                            last round);
@@ -308,7 +310,8 @@ const char *qr_status_string(qr_status st);
  * qr_device_error().  Nothing faults and nothing hangs. */
 qr_status qr_selftest_wait_timeout(unsigned int limit_us, void *stream);
 
-/* Self-test of the block-scale reciprocal the direct kernel uses (two
+/* Self-test of the block-scale reciprocal the direct path's allreduce
+ * kernels and the pipeline kernel at W = 2 and 4 use (two
  * Newton-Raphson steps on the hardware approximation instead of the
  * correctly rounded library reciprocal): writes, for every positive finite
  * fp16 value s (bit patterns 1 .. 0x7BFF in order), the binary32 reciprocal
