@@ -125,10 +125,10 @@ cudaError_t launch_pipe_cw(int cw, const PipeParams& p, cudaStream_t s) {
 // grid of resident CTAs looping over the message.  At W = 2 and 4 the
 // resident grid measured as fast or faster (up to 5 % at 128 MiB) and stays.
 // The direct path's kernel: the block kernel (one thread per block) for the
-// W = 2 two-stage calls of the integer formats, else the four-lanes-per-block
-// direct kernel.
+// W = 2 and W = 4 two-stage calls of the integer formats, else the
+// four-lanes-per-block direct kernel.
 template <int F, int M, int WS>
-constexpr bool kBlockKernelOf = WS == 2 && M == MODE_AR2 && FmtInfo<F>::quant && !FmtInfo<F>::fp8;
+constexpr bool kBlockKernelOf = (WS == 2 || WS == 4) && M == MODE_AR2 && FmtInfo<F>::quant && !FmtInfo<F>::fp8;
 
 template <int F, int D, int M, int WS>
 cudaError_t launch_dir_w(const PipeParams& p, cudaStream_t s) {
