@@ -289,7 +289,7 @@ def served_by(qr, W: int, dtype: int, fmt: int, stages: int, n: int) -> str:
     if path == qr.PATH_DIRECT:
         if stages == 0:
             return "qr_encode_kernel"
-        block = W in (2, 4) and stages == 2 and fmt not in (FP, FP8) and n >= (3 << 20 if W == 2 else 4 << 20)
+        block = W in (2, 4) and fmt not in (FP, FP8) and n >= (3 << 20 if W == 2 else 4 << 20)
         return "qr_block_kernel" if block else "qr_direct_kernel"
     return "qr_pipeline_kernel"
 

@@ -262,8 +262,8 @@ qr_status qr_allreduce_host(int W, qr_dtype dt, qr_format fmt, int stages,
  *   QR_PATH_DIRECT           single-pass kernels with one memory round trip
  *                            (lowest latency): four lanes per block, or one
  *                            thread per block for qr_quantize and for the W=2
- *                            and W=4 two-stage calls of the integer formats
- *                            from 3M / 4M elements per rank;
+ *                            and W=4 calls of the integer formats from 3M / 4M
+ *                            elements per rank;
  *   QR_PATH_PIPELINE_NARROW  the persistent bulk-copy pipeline with 8 KiB tiles
  *                            (mid-size messages: a shorter first fill and
  *                            last round);

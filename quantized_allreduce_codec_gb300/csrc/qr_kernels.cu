@@ -124,15 +124,15 @@ cudaError_t launch_pipe_cw(int cw, const PipeParams& p, cudaStream_t s) {
 // earlier ones retire: on GB300 3-5 % faster from 4 MiB per rank up than a
 // grid of resident CTAs looping over the message.  At W = 2 and 4 the
 // resident grid measured as fast or faster (up to 5 % at 128 MiB) and stays.
-// The direct path's kernel: for the W = 2 and W = 4 two-stage calls of the
-// integer formats the block kernel (one thread per block) from
-// kBlockMinElemsOf elements per rank up, else the four-lanes-per-block direct
-// kernel.  Below those sizes the block kernel has too few threads: at W = 4,
+// The direct path's kernel: for the W = 2 and W = 4 calls (one- and
+// two-stage) of the integer formats the block kernel (one thread per block)
+// from kBlockMinElemsOf elements per rank up, else the four-lanes-per-block
+// direct kernel.  Below those sizes the block kernel has too few threads: at W = 4,
 // 4 KiB-4 MiB per rank, it measured 0.3-0.8 us slower per call; the sizes are
 // the ones that minimise the summed relative excess over the selection
 // sweep's W = 2 and W = 4 two-stage integer shapes.
 template <int F, int M, int WS>
-constexpr bool kBlockKernelOf = (WS == 2 || WS == 4) && M == MODE_AR2 && FmtInfo<F>::quant && !FmtInfo<F>::fp8;
+constexpr bool kBlockKernelOf = (WS == 2 || WS == 4) && M != MODE_ENCODE && FmtInfo<F>::quant && !FmtInfo<F>::fp8;
 template <int WS>
 constexpr unsigned long long kBlockMinElemsOf = WS == 2 ? (3ull << 20) : (4ull << 20);
 

@@ -78,7 +78,7 @@ def kernels_launched(fn):
 
 def path_of(names):
     """The path a call took: PATH_DIRECT (qr_direct_kernel; qr_block_kernel for
-    the larger W=2 and W=4 two-stage calls of the integer formats; qr_encode_kernel for
+    the larger W=2 and W=4 calls of the integer formats; qr_encode_kernel for
     encode-only calls), else the pipeline with narrow or wide tiles (the
     pipeline kernel's fifth template argument: consumer warps per tile)."""
     kinds = {k for k, _ in names}
