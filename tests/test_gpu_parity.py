@@ -334,21 +334,23 @@ def test_paths_agree_past_the_table_limits(oracle_mod):
 
 
 @pytest.mark.parametrize("stages", [1, 2])
-@pytest.mark.parametrize("dtype", [F16, BF16])
+@pytest.mark.parametrize("dtype", [F16, BF16, qr.BF16_AS_F16])
 @pytest.mark.parametrize("fmt", [Q8, Q6, Q4, Q8A, Q4A])
 @pytest.mark.parametrize("W", [2, 4])
 def test_block_kernel_parity(oracle_mod, W, dtype, fmt, stages):
     """The direct path of a W=2 or W=4 call of an integer format runs the
     block kernel from 3M (W=2) or 4M (W=4) elements per rank: a message just
     past that size with a ragged tail gives the same bits as the wide-tile
-    pipeline (output and payload) and, on sampled blocks, as the oracle."""
-    rng = np.random.default_rng(7100 + 10 * W + fmt + 100 * dtype + 1000 * stages)
+    pipeline (output and payload) and, on sampled blocks, as the oracle
+    (fp16, bf16 and bf16 through fp16; the values stay inside the fp16
+    range, as the cast option requires)."""
+    rng = np.random.default_rng(7100 + 10 * W + fmt + 100 * int(dtype) + 1000 * stages)
     n = (4 << 20) + 40
     xs = []
     for _ in range(W):
         x = rng.standard_normal(n).astype(np.float32)
         x[rng.random(n) < 0.001] *= 50
-        xs.append(to_bits(x, dtype))
+        xs.append(to_bits(x, BF16 if dtype == qr.BF16_AS_F16 else dtype))  # the cast option takes bf16 messages
     with qr.forced_kernel_path(qr.PATH_DIRECT):
         out, wire = gpu_allreduce(dtype, fmt, stages, xs)
     with qr.forced_kernel_path(qr.PATH_PIPELINE):
