@@ -76,13 +76,14 @@ def test_two_stage_beyond_2_31_elements(oracle_mod, fmt):
     assert torch.equal(dec, out), "decoded payload differs from the output"
     del dec
 
-    # the direct kernel on the same inputs: the same output and payload
+    # the direct path on the same inputs (at this size the block kernel, one
+    # thread per block): the same output and payload
     out2 = torch.empty_like(out)
     wire2 = torch.empty_like(wire)
     with qr.forced_kernel_path(qr.PATH_DIRECT):
         qr.qr_allreduce_emulated(W, F16, fmt, 2, ins, n, out2, wire2)
         torch.cuda.synchronize()
-    assert torch.equal(out2, out), "direct and pipeline kernels disagree"
+    assert torch.equal(out2, out), "direct path and pipeline kernel disagree"
     assert torch.equal(wire2, wire), "direct and pipeline payloads disagree"
 
 
